@@ -1,0 +1,342 @@
+"""Benchmark of the speculative KV coder on GB300.
+
+One step = the whole hot path over one batch: encode the full synthetic KV
+cache (set-up, model + rANS encode, offset scan, compaction) and decode it
+back (set-up, CDF search + rANS decode). `value` is uncompressed KV bytes per
+second over encode + decode, device-timed with CUDA events on the coder's
+stream; the inputs (4.8 GB of KV and 4.8 GB of mu for the default workload)
+are far larger than the 129 MB L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl skv|reference]
+
+--impl reference times the CPU oracle (oracle/), the only reference there is
+for this method, on a bounded sample of the same workload.
+Under torchrun (N > 1) every rank codes its own full workload (weak scaling):
+chunks are independent, there is no data-path collective; only the barrier
+and the max-over-ranks timing use NCCL.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+# Algorithmic 32-bit operations per scalar ("Roofline"): the
+# format's own arithmetic for one scalar, counted once, search probes beyond
+# the two bracketing edges excluded.
+ALG_OPS = {("bf16", "encode"): 130, ("bf16", "decode"): 110,
+           ("e4m3", "encode"): 118, ("e4m3", "decode"): 98}
+SMS = 152               # GB300 streaming multiprocessors
+LANES_PER_SM_CLK = 128  # 4 schedulers x 32 lanes issue per clock
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return json.load(fh)
+    except OSError:
+        return {}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(prefix="skv_clocks_", suffix=".csv")
+        self.proc = None
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(gpu_index)], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    smax.append(float(p[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_oracle_run(cfg, sample_chunks: int, nthreads: int, seconds_hint: float = 0.0):
+    """Encode + decode `sample_chunks` chunks of the workload with the CPU oracle.
+
+    Returns (uncompressed bytes processed, seconds, description)."""
+    from lossless_kv_cache_scalar_gb300 import synth
+    from oracle import oracle as O
+    T = min(cfg.n_tokens, 256 * max(1, sample_chunks // 2))
+    sub = cfg.scaled(n_layers=1, n_tokens=T)
+    w = synth.to_numpy(synth.generate(sub))
+    lay = O.Layout(O.BF16 if cfg.dtype == "bf16" else O.E4M3, 1, sub.n_kv, sub.n_heads, sub.head_dim, T)
+    t0 = time.perf_counter()
+    s, offs = O.encode(lay, w["kv"], w["mu"], w["sigma"], w["counts"], nthreads=nthreads)
+    back = O.decode(lay, s, offs, w["mu"], w["sigma"], w["counts"], nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    assert np.array_equal(back, w["kv"].reshape(-1))
+    nbytes = lay.n_elems * sub.bytes_per_code
+    desc = (f"{O.num_chunks(lay)} chunks ({lay.n_elems} scalars) of the {cfg.name} recipe, "
+            f"1 layer x {sub.n_kv} x {T} tokens, encode+decode, oracle threads={nthreads}")
+    return nbytes, dt, desc
+
+
+def run_reference(args, cfg):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    from oracle import oracle as O
+    nthreads = O.threads()
+    total_b, total_t = 0, 0.0
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        b, t, desc = cpu_oracle_run(cfg, args.ref_chunks, nthreads)
+        if i >= args.warmup:
+            total_b += b
+            total_t += t
+    gbs = total_b / total_t / 1e9
+    line = {"metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32+f32",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": cfg.name, "sample": desc},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+METRIC = "KV encode+decode GB/s (uncompressed bytes) on GB300"
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="qwen3_8b")
+    ap.add_argument("--impl", default="skv", choices=["skv", "reference"])
+    ap.add_argument("--ref-chunks", type=int, default=8, help="chunks per oracle step")
+    ap.add_argument("--cpu-chunks", type=int, default=16, help="chunks in the cpu_baseline sample")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--traffic-json", default=os.path.join(ROOT, "profiles", "traffic.json"))
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "skv" else args.warmup
+
+    from lossless_kv_cache_scalar_gb300 import synth
+    cfg = synth.CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+
+    import lossless_kv_cache_scalar_gb300 as skv
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    cfg = cfg.scaled(seed=cfg.seed + 1000 * rank) if world > 1 else cfg
+    w = synth.generate(cfg, device=dev)
+    lay = skv.Layout(cfg.dtype, cfg.n_layers, cfg.n_kv, cfg.n_heads, cfg.head_dim, cfg.n_tokens)
+    coder = skv.Coder(lay, dev)
+    out, offsets = coder.alloc_output()
+    back = torch.empty_like(w["mu"])
+    stream = torch.cuda.Stream(device=dev)
+    n_el = lay.n_elems
+    raw_bytes = n_el * lay.bytes_per_code
+
+    def step(s):
+        coder.encode_into(w["kv"], w["mu"], w["sigma"], w["counts"], out, offsets, s)
+        coder.decode_into(out, offsets, w["mu"], w["sigma"], w["counts"], back, s)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step(stream)
+    coder.check_status("warmup", stream)
+    if not torch.equal(back, w["kv"]):
+        raise SystemExit("bench: decode did not restore the input")
+    total_bytes = int(offsets[-1].item())
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    barrier()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            coder.encode_into(w["kv"], w["mu"], w["sigma"], w["counts"], out, offsets, stream)
+            ev[i][1].record(stream)
+            coder.decode_into(out, offsets, w["mu"], w["sigma"], w["counts"], back, stream)
+            ev[i][2].record(stream)
+    barrier()
+    clocks = sampler.stop() if sampler else {}
+    coder.check_status("timed", stream)
+    t_enc = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+    t_dec = sum(e[1].elapsed_time(e[2]) for e in ev) / 1e3
+    t_tot = t_enc + t_dec
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([t_tot, t_enc, t_dec], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_tot, t_enc, t_dec = t.tolist()
+    value = world * raw_bytes * args.steps / t_tot / 1e9
+    enc_gbs = raw_bytes * args.steps / t_enc / 1e9
+    dec_gbs = raw_bytes * args.steps / t_dec / 1e9
+
+    # roofline of the dominant kernel (encode or decode call)
+    dom = "decode" if t_dec >= t_enc else "encode"
+    t_dom = (t_dec if dom == "decode" else t_enc) / args.steps
+    sm_mhz = clocks.get("sm_mhz") or _peaks().get("sm_max_mhz", 2070.0)
+    peak_tops = SMS * LANES_PER_SM_CLK * sm_mhz * 1e6 / 1e12
+    achieved = ALG_OPS[(lay.dtype, dom)] * n_el / t_dom / 1e12
+    traffic = None
+    try:
+        with open(args.traffic_json) as fh:
+            traffic = json.load(fh).get(f"{cfg.name}:{dom}")
+    except (OSError, ValueError):
+        traffic = None
+    hbm_peak = _peaks().get("hbm_gbs", 6685.5)
+    bits = 8.0 * total_bytes / n_el
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_run(coder, w, lay, args, dev, total_bytes)
+    line = None
+    if rank == 0:
+        cpu = None
+        try:
+            from oracle import oracle as O
+            nb, dt, desc = cpu_oracle_run(cfg, args.cpu_chunks, O.threads())
+            cpu = {"value": nb / dt / 1e9, "unit": "GB/s", "cores": O.threads(), "kind": "oracle",
+                   "sample": desc}
+        except Exception as e:  # the baseline must not hide the GPU number
+            cpu = {"value": None, "unit": "GB/s", "cores": None, "kind": "oracle", "sample": f"failed: {e}"}
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * t_tot / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u32/u64 int + f32", "data": "synthetic",
+            "config": {"workload": cfg.name, "shape": [cfg.n_layers, cfg.n_kv, cfg.n_tokens, cfg.n_heads,
+                                                       cfg.head_dim],
+                       "code_dtype": cfg.dtype, "scalars": n_el, "tokens_per_chunk": lay.tokens_per_chunk,
+                       "streams_per_chunk": lay.streams_per_chunk, "weights": list(lay.weights),
+                       "l2": "inputs 2 x %.1f GB >> 129 MB L2, no flush" % (raw_bytes / 1e9)},
+            "encode_gbs": enc_gbs, "decode_gbs": dec_gbs, "bits_per_scalar": bits,
+            "compression_ratio": 8.0 * lay.bytes_per_code / bits,
+            "roofline": {"bound": "alu", "kernel": dom, "achieved": achieved, "peak": peak_tops,
+                         "unit": "Tops/s", "frac": achieved / peak_tops, "traffic": traffic,
+                         "alg_ops_per_scalar": ALG_OPS[(lay.dtype, dom)],
+                         "peak_basis": f"{SMS} SMs x {LANES_PER_SM_CLK} lane-ops/clk x {sm_mhz:.0f} MHz (sampled)",
+                         "hbm_bound_gbs": hbm_peak * lay.bytes_per_code / (2 * lay.bytes_per_code + bits / 8),
+                         "hbm_peak_gbs": hbm_peak},
+            "roofline_encode_frac": ALG_OPS[(lay.dtype, "encode")] * n_el / (t_enc / args.steps) / 1e12 / peak_tops,
+            "roofline_decode_frac": ALG_OPS[(lay.dtype, "decode")] * n_el / (t_dec / args.steps) / 1e12 / peak_tops,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 6 * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e_run(coder, w, lay, args, dev, total_bytes):
+    """Same round trip with host (pinned) inputs and outputs copied inside the timed region."""
+    kv_h = w["kv"].cpu().pin_memory()
+    mu_h = w["mu"].cpu().pin_memory()
+    sig_h = w["sigma"].cpu().pin_memory()
+    cnt_h = w["counts"].cpu().pin_memory()
+    kv_d = torch.empty_like(w["kv"])
+    mu_d = torch.empty_like(w["mu"])
+    sig_d = torch.empty_like(w["sigma"])
+    cnt_d = torch.empty_like(w["counts"])
+    out, offsets = coder.alloc_output()
+    back = torch.empty_like(w["mu"])
+    bits_h = torch.empty(out.numel(), dtype=torch.uint8).pin_memory()
+    offs_h = torch.empty(offsets.numel(), dtype=torch.int64).pin_memory()
+    back_h = torch.empty(kv_h.shape, dtype=kv_h.dtype).pin_memory()
+    stream = torch.cuda.Stream(device=dev)
+    steps = max(1, min(args.steps, 3))
+    h2d = d2h = 0
+    with torch.cuda.stream(stream):
+        for i in range(1 + steps):
+            if i == 1:
+                stream.synchronize()
+                t0 = time.perf_counter()
+            kv_d.copy_(kv_h, non_blocking=True)
+            mu_d.copy_(mu_h, non_blocking=True)
+            sig_d.copy_(sig_h, non_blocking=True)
+            cnt_d.copy_(cnt_h, non_blocking=True)
+            coder.encode_into(kv_d, mu_d, sig_d, cnt_d, out, offsets, stream)
+            offs_h.copy_(offsets, non_blocking=True)
+            bits_h[:total_bytes].copy_(out[:total_bytes], non_blocking=True)
+            coder.decode_into(out, offsets, mu_d, sig_d, cnt_d, back, stream)
+            back_h.copy_(back, non_blocking=True)
+        stream.synchronize()
+        dt = time.perf_counter() - t0
+    coder.check_status("e2e", stream)
+    if not torch.equal(back_h, kv_h):
+        raise SystemExit("bench e2e: round trip through host buffers failed")
+    raw = lay.n_elems * lay.bytes_per_code
+    h2d = kv_h.numel() * kv_h.element_size() * 2 + sig_h.numel() * 4 + cnt_h.numel() * 8
+    d2h = total_bytes + offs_h.numel() * 8 + raw
+    return {"value": raw * steps / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps,
+            "timing": "host wall clock around pinned H2D copies, skv_encode, D2H of the bitstream, skv_decode, D2H of the KV"}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

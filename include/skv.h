@@ -1,0 +1,196 @@
+/*
+ * skv.h -- C ABI of the GB300 (sm_103a) speculative KV coder.
+ *
+ * The library entropy-codes every scalar of a KV cache against a predictor
+ * and decodes it back bit for bit. The method is the one of the
+ * "Speculative KV Coding" wiki (aisparkup.com): both ends hold the
+ * predictor's per-element mean mu and a per-(layer, kv, head, channel) scale
+ * sigma (pipeline section); each scalar is coded under the mixture
+ *     q(x) = 0.95 N(x; mu, sigma^2) + 0.03 N(x; mu, (3 sigma)^2) + 0.02 p_hat(x)
+ * with p_hat the empirical marginal of the codes (mixture section); the code
+ * length approaches -log2 q(x) (information-theory section of the blog
+ * "推测性KV编码：用预测模型实现缓存无损压缩4倍", blog.hotdry.top), and the
+ * CDF must be bit-identical at both ends (that blog's deployment section).
+ * The integer discretisation and the bitstream are specified in FORMAT.md
+ * (version 1).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named as device pointers must point to device memory of the
+ *    current CUDA device; the caller allocates and frees all memory (inputs,
+ *    outputs, workspace). The library never allocates, frees or retains
+ *    caller memory.
+ *  - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is the
+ *    legacy default stream) and is asynchronous: read outputs and *status
+ *    after synchronising that stream.
+ *  - The return value reports argument and launch errors found on the host
+ *    (SKV_OK, SKV_ERR_INVALID_ARG, SKV_ERR_CUDA); nothing is enqueued when it
+ *    is not SKV_OK. Data-dependent errors are written by the device to the
+ *    int32 at `status` (device memory), which the call first sets to SKV_OK;
+ *    the first error found wins. The device never traps.
+ *  - Tensor layout is canonical: KV and mu are [n_layers][n_kv][n_tokens]
+ *    [n_heads][head_dim] codes, channel fastest, 16-byte aligned; sigma is
+ *    float32 [n_layers][n_kv][n_heads][head_dim]; counts is uint64[N], N =
+ *    65536 (bf16) or 256 (e4m3), indexed by code bit pattern.
+ */
+#ifndef SKV_H
+#define SKV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SKV_FORMAT_VERSION 1u
+
+/* Code types (FORMAT.md section 1). */
+enum { SKV_BF16 = 0, SKV_E4M3 = 1 };
+
+/* Status codes: returned by calls (host-detected) or written to *status (device-detected). */
+enum {
+    SKV_OK = 0,
+    SKV_ERR_INVALID_ARG = 1,    /* bad layout, pointer, alignment, size or chunk id      */
+    SKV_ERR_CUDA = 2,           /* a CUDA call or launch failed                           */
+    SKV_ERR_NONFINITE_MU = 3,   /* some mu code is NaN or infinite (modelled as 0)         */
+    SKV_ERR_BAD_SIGMA = 4,      /* some sigma is non-finite or below 2^-126                */
+    SKV_ERR_EMPTY_MARGINAL = 5, /* w_marginal > 0 but the counts sum to 0                  */
+    SKV_ERR_CAPACITY = 6,       /* the encoded stream does not fit out_capacity            */
+    SKV_ERR_CORRUPT = 7,        /* bitstream or offsets inconsistent (decode)              */
+    SKV_ERR_TIMEOUT = 8         /* reserved: a bounded device wait ran out                 */
+};
+
+/*
+ * What is coded and how it is cut (FORMAT.md section 7).
+ *  version            SKV_FORMAT_VERSION
+ *  dtype              SKV_BF16 or SKV_E4M3
+ *  n_layers, n_kv     planes; n_kv is 2 for K and V
+ *  n_heads, head_dim  HD = n_heads * head_dim channels; HD * bytes_per_code % 16 == 0
+ *  n_tokens           T (may be 0)
+ *  tokens_per_chunk   page length T_c >= 1; a chunk is one (layer, kv, page) and
+ *                     decodes independently (the random-access unit)
+ *  streams_per_chunk  W = 32 * G, G in 1..8: interleaved rANS streams per chunk
+ *  w_narrow, w_wide, w_marginal  integer mixture weights, sum 100 (the wiki's
+ *                     0.95 / 0.03 / 0.02 are 95 / 3 / 2)
+ */
+typedef struct skv_layout {
+    uint32_t version;
+    uint32_t dtype;
+    uint32_t n_layers;
+    uint32_t n_kv;
+    uint32_t n_heads;
+    uint32_t head_dim;
+    uint64_t n_tokens;
+    uint32_t tokens_per_chunk;
+    uint32_t streams_per_chunk;
+    uint32_t w_narrow;
+    uint32_t w_wide;
+    uint32_t w_marginal;
+    uint32_t reserved;          /* must be 0 */
+} skv_layout;
+
+/* Library build/format version: returns SKV_FORMAT_VERSION. */
+uint32_t skv_version(void);
+
+/* Name of a status code ("OK", "CORRUPT", ...); never NULL. */
+const char *skv_status_string(int32_t status);
+
+/*
+ * Fill *lay with the given shape and the defaults: tokens_per_chunk 256,
+ * streams_per_chunk 64, weights 95/3/2 (the wiki's mixture section).
+ * Returns SKV_ERR_INVALID_ARG if lay is NULL or the shape is invalid.
+ */
+int32_t skv_layout_init(skv_layout *lay, uint32_t dtype, uint32_t n_layers, uint32_t n_kv,
+                        uint32_t n_heads, uint32_t head_dim, uint64_t n_tokens);
+
+/* Host-side validation of a layout: SKV_OK or SKV_ERR_INVALID_ARG. */
+int32_t skv_layout_check(const skv_layout *lay);
+
+/* Number of chunks n = n_layers * n_kv * ceil(n_tokens / tokens_per_chunk). */
+int32_t skv_num_chunks(const skv_layout *lay, uint64_t *n_chunks);
+
+/*
+ * Upper bound on the encoded size in bytes (FORMAT.md section 8): an
+ * out_capacity of this size never gives SKV_ERR_CAPACITY. About 1.56x the
+ * raw bf16 bytes and 2.1x the raw e4m3 bytes, reached only by data the model
+ * predicts very badly.
+ */
+int32_t skv_max_encoded_bytes(const skv_layout *lay, uint64_t *bytes);
+
+/*
+ * Device workspace bytes needed by skv_encode (encode != 0) or by
+ * skv_decode / skv_decode_chunks (encode == 0). The workspace must be
+ * 256-byte aligned and must not be used by another call in flight.
+ * Encode holds one worst-case word slot per stream group (about the size of
+ * skv_max_encoded_bytes); decode holds only the tables (< 1 MB).
+ */
+int32_t skv_workspace_bytes(const skv_layout *lay, int32_t encode, uint64_t *bytes);
+
+/*
+ * Encode a whole KV cache (the encoder of the wiki's pipeline section).
+ *  kv, mu        device, codes in canonical layout (uint16 bf16 / uint8 e4m3), 16-byte aligned
+ *  sigma         device float32 [n_layers][n_kv][n_heads][head_dim]
+ *  counts        device uint64[N], the marginal histogram (may be NULL iff w_marginal == 0);
+ *                its sum must be below 2^63
+ *  out           device, out_capacity bytes, 16-byte aligned: receives the chunks back to back
+ *  offsets       device uint64[n_chunks + 1]: offsets[k] = byte start of chunk k,
+ *                offsets[n_chunks] = total encoded bytes
+ *  status        device int32
+ *  workspace     device, ws_bytes >= skv_workspace_bytes(lay, 1)
+ * Device errors: NONFINITE_MU, BAD_SIGMA, EMPTY_MARGINAL, CAPACITY (offsets
+ * are still complete; chunks that do not fit are not written).
+ */
+int32_t skv_encode(const skv_layout *lay, const void *kv, const void *mu, const float *sigma,
+                   const uint64_t *counts, void *out, uint64_t out_capacity, uint64_t *offsets,
+                   int32_t *status, void *workspace, uint64_t ws_bytes, void *stream);
+
+/*
+ * Decode a whole bitstream back to KV codes (the decoder of the wiki's
+ * pipeline section: bits plus (mu, sigma) restore KV_full exactly).
+ *  bitstream     device, bitstream_bytes bytes, 16-byte aligned
+ *  offsets       device uint64[n_chunks + 1] as written by skv_encode
+ *  mu, sigma, counts   exactly as given to skv_encode
+ *  kv_out        device, codes in canonical layout, 16-byte aligned
+ *  workspace     device, ws_bytes >= skv_workspace_bytes(lay, 0)
+ * Device errors: CORRUPT (the chunk's output is then unspecified),
+ * NONFINITE_MU, BAD_SIGMA, EMPTY_MARGINAL.
+ */
+int32_t skv_decode(const skv_layout *lay, const void *bitstream, uint64_t bitstream_bytes,
+                   const uint64_t *offsets, const void *mu, const float *sigma,
+                   const uint64_t *counts, void *kv_out, int32_t *status, void *workspace,
+                   uint64_t ws_bytes, void *stream);
+
+/*
+ * Random-access decode of selected chunks (pages) of a full bitstream, for
+ * the offload and long-context uses the wiki lists (uses section).
+ *  chunk_ids     device uint32[n_ids], each < n_chunks (else SKV_ERR_INVALID_ARG on *status)
+ *  pages_out     device, n_ids * tokens_per_chunk * HD codes, 16-byte aligned; chunk
+ *                chunk_ids[i] is written at pages_out + i * tokens_per_chunk * HD codes,
+ *                in its own [token][head][channel] order (a shorter last page leaves
+ *                the rest of its slot untouched)
+ * Other arguments as skv_decode.
+ */
+int32_t skv_decode_chunks(const skv_layout *lay, const void *bitstream, uint64_t bitstream_bytes,
+                          const uint64_t *offsets, const void *mu, const float *sigma,
+                          const uint64_t *counts, const uint32_t *chunk_ids, uint32_t n_ids,
+                          void *pages_out, int32_t *status, void *workspace, uint64_t ws_bytes,
+                          void *stream);
+
+/*
+ * Evaluate the model's cumulative frequency C(o) (FORMAT.md section 5) for n
+ * independent queries: C[i] = C(ords[i]) for predictor code mu_codes[i] and
+ * scale sigmas[i], under the weights of lay and the marginal counts. For
+ * checking the model kernel against an independent implementation.
+ *  mu_codes (uint32, code in the low bits), sigmas (float32), ords (uint32, 0..N),
+ *  C_out (uint32): device arrays of n entries. workspace >= skv_workspace_bytes(lay, 0).
+ * Device errors: NONFINITE_MU, BAD_SIGMA, EMPTY_MARGINAL.
+ */
+int32_t skv_cdf_eval(const skv_layout *lay, const uint64_t *counts, uint64_t n,
+                     const uint32_t *mu_codes, const float *sigmas, const uint32_t *ords,
+                     uint32_t *C_out, int32_t *status, void *workspace, uint64_t ws_bytes,
+                     void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SKV_H */

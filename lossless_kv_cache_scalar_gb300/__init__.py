@@ -1,0 +1,9 @@
+"""GB300-native speculative KV coding: lossless entropy coding of KV-cache
+scalars against a predictor (mu, sigma) under the three-component mixture of
+the Speculative KV Coding wiki. The work runs in libskv.so (include/skv.h);
+this package is its binding and the seeded synthetic workloads.
+"""
+from ._binding import SKVError, SKV_BF16, SKV_E4M3, STATUS_NAMES, lib  # noqa: F401
+from .api import Coder, Layout, cdf_eval, decode, decode_chunks, encode  # noqa: F401
+
+__all__ = ["Coder", "Layout", "SKVError", "cdf_eval", "decode", "decode_chunks", "encode", "lib"]

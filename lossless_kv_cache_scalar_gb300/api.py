@@ -1,0 +1,216 @@
+"""PyTorch-facing wrapper of the C ABI: device buffers, streams and status words.
+
+PyTorch only provides device memory and streams here; encoding and decoding
+run in libskv.so's kernels (skv_encode / skv_decode / skv_decode_chunks /
+skv_cdf_eval), called through the ctypes binding with raw device pointers.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+
+import torch
+
+from . import _binding as B
+
+_DT = {"bf16": B.SKV_BF16, "e4m3": B.SKV_E4M3}
+
+
+@dataclass
+class Layout:
+    """Shape and coding parameters (the skv_layout struct of include/skv.h)."""
+    dtype: str
+    n_layers: int
+    n_kv: int
+    n_heads: int
+    head_dim: int
+    n_tokens: int
+    tokens_per_chunk: int = 256
+    streams_per_chunk: int = 64
+    weights: tuple = (95, 3, 2)
+
+    def c(self) -> B.skv_layout:
+        w = self.weights
+        return B.skv_layout(B.SKV_FORMAT_VERSION, _DT[self.dtype], self.n_layers, self.n_kv,
+                            self.n_heads, self.head_dim, self.n_tokens, self.tokens_per_chunk,
+                            self.streams_per_chunk, w[0], w[1], w[2], 0)
+
+    @property
+    def n_codes(self) -> int:
+        return 65536 if self.dtype == "bf16" else 256
+
+    @property
+    def bytes_per_code(self) -> int:
+        return 2 if self.dtype == "bf16" else 1
+
+    @property
+    def n_elems(self) -> int:
+        return self.n_layers * self.n_kv * self.n_tokens * self.n_heads * self.head_dim
+
+    @property
+    def page_elems(self) -> int:
+        return self.tokens_per_chunk * self.n_heads * self.head_dim
+
+    def _q(self, fn, *extra) -> int:
+        v = C.c_uint64()
+        B.check(fn.__name__, fn(C.byref(self.c()), *extra, C.byref(v)))
+        return v.value
+
+    @property
+    def n_chunks(self) -> int:
+        return self._q(B.lib().skv_num_chunks)
+
+    @property
+    def max_encoded_bytes(self) -> int:
+        return self._q(B.lib().skv_max_encoded_bytes)
+
+    def workspace_bytes(self, encode: bool) -> int:
+        return self._q(B.lib().skv_workspace_bytes, 1 if encode else 0)
+
+    @classmethod
+    def for_tensor(cls, kv: torch.Tensor, dtype: str | None = None, **kw) -> "Layout":
+        L, K, T, H, D = kv.shape
+        if dtype is None:
+            dtype = "bf16" if kv.element_size() == 2 else "e4m3"
+        return cls(dtype, L, K, H, D, T, **kw)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream: torch.cuda.Stream | None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def _check_codes(t: torch.Tensor, lay: Layout, what: str):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{what} must be a contiguous CUDA tensor")
+    if t.element_size() != lay.bytes_per_code or t.numel() != lay.n_elems:
+        raise ValueError(f"{what}: expected {lay.n_elems} codes of {lay.bytes_per_code} bytes")
+
+
+class Coder:
+    """Encoder/decoder for one layout, holding its workspace and status word.
+
+    One Coder must not run two calls at once on different streams (they would
+    share the workspace).
+    """
+
+    def __init__(self, layout: Layout, device: torch.device | str | int = "cuda",
+                 encode: bool = True, decode: bool = True):
+        self.layout = layout
+        self.device = torch.device(device)
+        self._c = layout.c()
+        need = 0
+        if encode:
+            need = max(need, layout.workspace_bytes(True))
+        if decode:
+            need = max(need, layout.workspace_bytes(False))
+        self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.n_chunks = layout.n_chunks
+
+    # -- status
+    def check_status(self, where: str, stream=None):
+        (stream or torch.cuda.current_stream()).synchronize()
+        st = int(self.status.item())
+        if st:
+            raise B.SKVError(where, st)
+
+    def alloc_output(self):
+        cap = self.layout.max_encoded_bytes
+        out = torch.empty(max(cap, 16), dtype=torch.uint8, device=self.device)
+        offsets = torch.empty(self.n_chunks + 1, dtype=torch.int64, device=self.device)
+        return out, offsets
+
+    # -- encode
+    def encode_into(self, kv, mu, sigma, counts, out, offsets, stream=None):
+        """Enqueue skv_encode; no synchronisation."""
+        lay = self.layout
+        _check_codes(kv, lay, "kv")
+        _check_codes(mu, lay, "mu")
+        rc = B.lib().skv_encode(C.byref(self._c), _ptr(kv), _ptr(mu), _ptr(sigma), _ptr(counts),
+                                _ptr(out), out.numel(), _ptr(offsets), _ptr(self.status),
+                                _ptr(self.workspace), self.workspace.numel(),
+                                _stream_handle(stream))
+        B.check("skv_encode", rc)
+
+    def encode(self, kv, mu, sigma, counts, stream=None):
+        """Encode and check. Returns (bitstream uint8 tensor, offsets int64 tensor)."""
+        out, offsets = self.alloc_output()
+        self.encode_into(kv, mu, sigma, counts, out, offsets, stream)
+        self.check_status("skv_encode", stream)
+        total = int(offsets[-1].item())
+        return out[:total], offsets
+
+    # -- decode
+    def decode_into(self, bitstream, offsets, mu, sigma, counts, kv_out, stream=None):
+        lay = self.layout
+        _check_codes(mu, lay, "mu")
+        _check_codes(kv_out, lay, "kv_out")
+        rc = B.lib().skv_decode(C.byref(self._c), _ptr(bitstream), bitstream.numel(),
+                                _ptr(offsets), _ptr(mu), _ptr(sigma), _ptr(counts), _ptr(kv_out),
+                                _ptr(self.status), _ptr(self.workspace), self.workspace.numel(),
+                                _stream_handle(stream))
+        B.check("skv_decode", rc)
+
+    def decode(self, bitstream, offsets, mu, sigma, counts, stream=None):
+        kv = torch.empty_like(mu)
+        self.decode_into(bitstream, offsets, mu, sigma, counts, kv, stream)
+        self.check_status("skv_decode", stream)
+        return kv
+
+    def decode_chunks_into(self, bitstream, offsets, mu, sigma, counts, chunk_ids, pages_out,
+                           stream=None):
+        lay = self.layout
+        ids = chunk_ids
+        if ids.dtype != torch.int32 or not ids.is_cuda:
+            raise ValueError("chunk_ids must be an int32 CUDA tensor")
+        if pages_out.numel() != ids.numel() * lay.page_elems:
+            raise ValueError("pages_out must hold n_ids * tokens_per_chunk * HD codes")
+        rc = B.lib().skv_decode_chunks(C.byref(self._c), _ptr(bitstream), bitstream.numel(),
+                                       _ptr(offsets), _ptr(mu), _ptr(sigma), _ptr(counts), _ptr(ids),
+                                       ids.numel(), _ptr(pages_out), _ptr(self.status),
+                                       _ptr(self.workspace), self.workspace.numel(),
+                                       _stream_handle(stream))
+        B.check("skv_decode_chunks", rc)
+
+    def decode_chunks(self, bitstream, offsets, mu, sigma, counts, chunk_ids, stream=None):
+        lay = self.layout
+        pages = torch.zeros((chunk_ids.numel(), lay.page_elems), dtype=mu.dtype, device=mu.device)
+        self.decode_chunks_into(bitstream, offsets, mu, sigma, counts, chunk_ids, pages, stream)
+        self.check_status("skv_decode_chunks", stream)
+        return pages
+
+
+def cdf_eval(layout: Layout, counts, mu_codes, sigmas, ords, stream=None) -> torch.Tensor:
+    """C(o) per query via skv_cdf_eval (uint32 results as int64 tensor)."""
+    dev = mu_codes.device
+    n = ords.numel()
+    ws = torch.empty(max(layout.workspace_bytes(False), 256), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.empty(n, dtype=torch.int32, device=dev)
+    rc = B.lib().skv_cdf_eval(C.byref(layout.c()), _ptr(counts), n, _ptr(mu_codes), _ptr(sigmas),
+                              _ptr(ords), _ptr(out), _ptr(status), _ptr(ws), ws.numel(),
+                              _stream_handle(stream))
+    B.check("skv_cdf_eval", rc)
+    (stream or torch.cuda.current_stream()).synchronize()
+    st = int(status.item())
+    if st:
+        raise B.SKVError("skv_cdf_eval", st)
+    return out.to(torch.int64) & 0xFFFFFFFF
+
+
+def encode(layout: Layout, kv, mu, sigma, counts, stream=None):
+    return Coder(layout, kv.device, decode=False).encode(kv, mu, sigma, counts, stream)
+
+
+def decode(layout: Layout, bitstream, offsets, mu, sigma, counts, stream=None):
+    return Coder(layout, mu.device, encode=False).decode(bitstream, offsets, mu, sigma, counts, stream)
+
+
+def decode_chunks(layout: Layout, bitstream, offsets, mu, sigma, counts, chunk_ids, stream=None):
+    return Coder(layout, mu.device, encode=False).decode_chunks(bitstream, offsets, mu, sigma,
+                                                                counts, chunk_ids, stream)

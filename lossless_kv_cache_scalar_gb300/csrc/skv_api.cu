@@ -1,0 +1,399 @@
+// skv_api.cu -- the C ABI (include/skv.h): argument checks, workspace layout,
+// the per-call set-up kernel (sigma -> 1/sigma, marginal counts -> P_hat
+// table) and the launches of the encoder and decoder kernels.
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "skv_model.cuh"
+
+namespace skv {
+
+int launch_encode(const EncArgs &a, cudaStream_t st);
+int launch_scan(const ScanArgs &a, cudaStream_t st);
+int launch_compact(const CompactArgs &a, cudaStream_t st);
+int launch_decode(const DecArgs &a, cudaStream_t st);
+
+// ------------------------------------------------------------- set-up kernel
+
+// P_hat(o) = floor(2^24 cum(o) / total) exactly (FORMAT.md section 5): a
+// binary64 estimate, then integer correction with 128-bit products.
+__device__ uint32_t phat_entry(uint64_t cum, uint64_t total) {
+    const unsigned __int128 lhs = (unsigned __int128)cum << 24;
+    double est = (double)cum / (double)total * 16777216.0;
+    uint32_t p = est >= 16777216.0 ? 16777216u : (uint32_t)est;
+    while (p < 16777216u && (unsigned __int128)(p + 1u) * total <= lhs) ++p;
+    while (p > 0u && (unsigned __int128)p * total > lhs) --p;
+    return p;
+}
+
+// One CTA: validates sigma and writes rsig = fl32(1/sigma); builds P_hat in
+// code order from the marginal histogram.
+template <uint32_t DT>
+__global__ void __launch_bounds__(1024) setup_kernel(const SetupArgs a) {
+    using K = Codes<DT>;
+    const Geom &g = a.g;
+    const uint32_t tid = threadIdx.x;
+    __shared__ uint64_t warp_tot[32];
+    __shared__ int bad_sigma;
+    if (tid == 0) bad_sigma = 0;
+    __syncthreads();
+
+    const uint64_t nsig = g.n_planes * g.HD;
+    for (uint64_t i = tid; i < nsig; i += blockDim.x) {
+        const float sg = a.sigma[i];
+        const bool ok = isfinite(sg) && sg >= 1.17549435e-38f;   // 2^-126
+        a.rsig[i] = ok ? __frcp_rn(sg) : 1.0f;
+        if (!ok) bad_sigma = 1;
+    }
+
+    if (g.w_h == 0) {
+        for (uint32_t o = tid; o <= K::N; o += blockDim.x) a.phat[o] = 0u;
+    } else {
+        constexpr uint32_t per = (K::N + 1023u) / 1024u;
+        const uint32_t o0 = tid * per, o1 = min(o0 + per, K::N);
+        uint64_t local = 0;
+        for (uint32_t o = o0; o < o1; ++o) local += a.counts[K::code(o)];
+        const uint32_t lane = tid & 31u, warp = tid >> 5;
+        uint64_t incl = local;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint64_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+            if (lane >= (uint32_t)d) incl += v;
+        }
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            uint64_t t = warp_tot[lane];
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const uint64_t v = __shfl_up_sync(0xFFFFFFFFu, t, d);
+                if (lane >= (uint32_t)d) t += v;
+            }
+            warp_tot[lane] = t;
+        }
+        __syncthreads();
+        const uint64_t total = warp_tot[31];
+        uint64_t cum = (warp ? warp_tot[warp - 1] : 0ull) + incl - local;
+        if (total == 0) {
+            for (uint32_t o = tid; o <= K::N; o += blockDim.x) a.phat[o] = 0u;
+            if (tid == 0) set_status(a.status, SKV_ERR_EMPTY_MARGINAL);
+        } else {
+            for (uint32_t o = o0; o < o1; ++o) {
+                a.phat[o] = phat_entry(cum, total);
+                cum += a.counts[K::code(o)];
+            }
+            if (tid == 0) a.phat[K::N] = 1u << 24;
+        }
+    }
+    __syncthreads();
+    if (tid == 0 && bad_sigma) set_status(a.status, SKV_ERR_BAD_SIGMA);
+}
+
+// C(o) for independent (mu, sigma, o) queries (model-kernel checks).
+template <uint32_t DT>
+__global__ void __launch_bounds__(256) cdf_eval_kernel(const CdfArgs a) {
+    using K = Codes<DT>;
+    __shared__ Tables tab;
+    __shared__ Tables8 tab8;
+    stage_tables<DT>(tab, tab8, a.phat);
+    const Weights w{a.g.w_n, a.g.w_w, a.g.w_h};
+    bool bad_mu = false, bad_sig = false;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < a.n;
+         i += (uint64_t)gridDim.x * blockDim.x) {
+        const uint32_t mc = a.mu_codes[i] & (K::N - 1u);
+        const float sg = a.sigmas[i];
+        const bool ok = isfinite(sg) && sg >= 1.17549435e-38f;
+        bad_sig |= !ok;
+        const float rs = ok ? __frcp_rn(sg) : 1.0f;
+        const bool fin = K::finite(mc);
+        bad_mu |= !fin;
+        const float mu = fin ? K::value(mc) : 0.0f;
+        const uint32_t o = min(a.ords[i], K::N);
+        a.C[i] = (o == K::N) ? (1u << K::m) : cdf<DT>(tab, &tab8, w, a.phat, o, mu, rs);
+    }
+    if (bad_sig) set_status(a.status, SKV_ERR_BAD_SIGMA);
+    if (bad_mu) set_status(a.status, SKV_ERR_NONFINITE_MU);
+}
+
+// --------------------------------------------------------------- host side
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+static int32_t make_geom(const skv_layout *lay, Geom &g) {
+    if (!lay || lay->version != SKV_FORMAT_VERSION || lay->reserved != 0) return SKV_ERR_INVALID_ARG;
+    if (lay->dtype != SKV_BF16 && lay->dtype != SKV_E4M3) return SKV_ERR_INVALID_ARG;
+    if (!lay->n_layers || !lay->n_kv || !lay->n_heads || !lay->head_dim) return SKV_ERR_INVALID_ARG;
+    if (!lay->tokens_per_chunk) return SKV_ERR_INVALID_ARG;
+    const uint32_t W = lay->streams_per_chunk;
+    if (W == 0 || W % 32 != 0 || W > 256) return SKV_ERR_INVALID_ARG;
+    if (lay->w_narrow + lay->w_wide + lay->w_marginal != 100u) return SKV_ERR_INVALID_ARG;
+    const DtypeInfo d = dtype_info(lay->dtype);
+    const uint64_t HD = (uint64_t)lay->n_heads * lay->head_dim;
+    if ((HD * d.bytes) % 16 != 0 || HD > (1ull << 24)) return SKV_ERR_INVALID_ARG;
+    if (lay->n_tokens > (1ull << 40)) return SKV_ERR_INVALID_ARG;
+    std::memset(&g, 0, sizeof g);
+    g.dtype = lay->dtype;
+    g.n_kv = lay->n_kv;
+    g.HD = (uint32_t)HD;
+    g.W = W;
+    g.G = W / 32;
+    g.Tc = lay->tokens_per_chunk;
+    g.T = lay->n_tokens;
+    g.P = (lay->n_tokens + lay->tokens_per_chunk - 1) / lay->tokens_per_chunk;
+    g.n_planes = (uint64_t)lay->n_layers * lay->n_kv;
+    g.n_chunks = g.n_planes * g.P;
+    g.n_groups = g.n_chunks * g.G;
+    g.w_n = lay->w_narrow;
+    g.w_w = lay->w_wide;
+    g.w_h = lay->w_marginal;
+    g.hdr_bytes = (uint32_t)(8ull * W + pad16(4ull * g.G));
+    // scratch words per group: the longest stream of a full chunk bounds all
+    const uint64_t ntok_full = g.T < g.Tc ? g.T : g.Tc;
+    const uint64_t nvec_full = ntok_full * HD / d.V;
+    const uint64_t nmax = stream_vectors(g, nvec_full, 0) * d.V;
+    g.cap_words = 32ull * ((nmax * (d.m + 1) + 31) / 32);
+    if (g.cap_words > 0xFFFFFFF0ull) return SKV_ERR_INVALID_ARG;
+    return SKV_OK;
+}
+
+// Worst-case bytes of one chunk with n_vec vectors (FORMAT.md section 8).
+static uint64_t chunk_max_bytes(const Geom &g, uint64_t n_vec) {
+    const DtypeInfo d = dtype_info(g.dtype);
+    uint64_t b = g.hdr_bytes;
+    for (uint32_t j = 0; j < g.G; ++j) {
+        const uint64_t nmax = stream_vectors(g, n_vec, 32 * j) * d.V;
+        b += pad16(4ull * 32ull * ((nmax * (d.m + 1) + 31) / 32));
+    }
+    return b;
+}
+
+struct Workspace {
+    uint32_t *phat;
+    float *rsig;
+    uint64_t *states;
+    uint32_t *nwords;
+    uint32_t *scratch;
+    uint64_t bytes;
+};
+
+static uint64_t round256(uint64_t b) { return (b + 255u) & ~uint64_t(255); }
+
+static Workspace carve(const Geom &g, bool encode, uint8_t *base) {
+    // offsets are computed as integers and only then turned into pointers
+    const DtypeInfo d = dtype_info(g.dtype);
+    uint64_t off = 0, o_phat, o_rsig, o_states = 0, o_nwords = 0, o_scratch = 0;
+    o_phat = off;
+    off += round256(4ull * (d.N + 1));
+    o_rsig = off;
+    off += round256(4ull * g.n_planes * g.HD);
+    if (encode) {
+        o_states = off;
+        off += round256(8ull * 32ull * g.n_groups);
+        o_nwords = off;
+        off += round256(4ull * g.n_groups);
+        o_scratch = off;
+        off += round256(4ull * g.cap_words * g.n_groups);
+    }
+    Workspace w{};
+    w.bytes = off;
+    if (base) {
+        w.phat = reinterpret_cast<uint32_t *>(base + o_phat);
+        w.rsig = reinterpret_cast<float *>(base + o_rsig);
+        if (encode) {
+            w.states = reinterpret_cast<uint64_t *>(base + o_states);
+            w.nwords = reinterpret_cast<uint32_t *>(base + o_nwords);
+            w.scratch = reinterpret_cast<uint32_t *>(base + o_scratch);
+        }
+    }
+    return w;
+}
+
+static int32_t run_setup(const Geom &g, const float *sigma, const uint64_t *counts,
+                         const Workspace &ws, int32_t *status, cudaStream_t st) {
+    SetupArgs s{g, sigma, counts, ws.phat, ws.rsig, status};
+    if (g.dtype == SKV_BF16) setup_kernel<SKV_BF16><<<1, 1024, 0, st>>>(s);
+    else setup_kernel<SKV_E4M3><<<1, 1024, 0, st>>>(s);
+    return cudaGetLastError() == cudaSuccess ? SKV_OK : SKV_ERR_CUDA;
+}
+
+static int32_t common_checks(const Geom &g, const float *sigma, const uint64_t *counts,
+                             int32_t *status, void *workspace, uint64_t ws_bytes, bool encode) {
+    if (!sigma || !status || !workspace) return SKV_ERR_INVALID_ARG;
+    if (g.w_h && !counts) return SKV_ERR_INVALID_ARG;
+    if (((uintptr_t)workspace & 255u) != 0) return SKV_ERR_INVALID_ARG;
+    if (ws_bytes < carve(g, encode, nullptr).bytes) return SKV_ERR_INVALID_ARG;
+    return SKV_OK;
+}
+
+}  // namespace skv
+
+using namespace skv;
+
+extern "C" {
+
+uint32_t skv_version(void) { return SKV_FORMAT_VERSION; }
+
+const char *skv_status_string(int32_t s) {
+    switch (s) {
+        case SKV_OK: return "OK";
+        case SKV_ERR_INVALID_ARG: return "INVALID_ARG";
+        case SKV_ERR_CUDA: return "CUDA";
+        case SKV_ERR_NONFINITE_MU: return "NONFINITE_MU";
+        case SKV_ERR_BAD_SIGMA: return "BAD_SIGMA";
+        case SKV_ERR_EMPTY_MARGINAL: return "EMPTY_MARGINAL";
+        case SKV_ERR_CAPACITY: return "CAPACITY";
+        case SKV_ERR_CORRUPT: return "CORRUPT";
+        case SKV_ERR_TIMEOUT: return "TIMEOUT";
+        default: return "UNKNOWN";
+    }
+}
+
+int32_t skv_layout_init(skv_layout *lay, uint32_t dtype, uint32_t n_layers, uint32_t n_kv,
+                        uint32_t n_heads, uint32_t head_dim, uint64_t n_tokens) {
+    if (!lay) return SKV_ERR_INVALID_ARG;
+    std::memset(lay, 0, sizeof *lay);
+    lay->version = SKV_FORMAT_VERSION;
+    lay->dtype = dtype;
+    lay->n_layers = n_layers;
+    lay->n_kv = n_kv;
+    lay->n_heads = n_heads;
+    lay->head_dim = head_dim;
+    lay->n_tokens = n_tokens;
+    lay->tokens_per_chunk = 256;
+    lay->streams_per_chunk = 64;
+    lay->w_narrow = 95;
+    lay->w_wide = 3;
+    lay->w_marginal = 2;
+    return skv_layout_check(lay);
+}
+
+int32_t skv_layout_check(const skv_layout *lay) {
+    Geom g;
+    return make_geom(lay, g);
+}
+
+int32_t skv_num_chunks(const skv_layout *lay, uint64_t *n_chunks) {
+    Geom g;
+    const int32_t r = make_geom(lay, g);
+    if (r != SKV_OK || !n_chunks) return SKV_ERR_INVALID_ARG;
+    *n_chunks = g.n_chunks;
+    return SKV_OK;
+}
+
+int32_t skv_max_encoded_bytes(const skv_layout *lay, uint64_t *bytes) {
+    Geom g;
+    if (make_geom(lay, g) != SKV_OK || !bytes) return SKV_ERR_INVALID_ARG;
+    if (g.n_chunks == 0) { *bytes = 0; return SKV_OK; }
+    const DtypeInfo d = dtype_info(g.dtype);
+    const uint64_t full = chunk_max_bytes(g, (uint64_t)g.Tc * g.HD / d.V);
+    const uint64_t last_tok = g.T - (g.P - 1) * g.Tc;
+    const uint64_t last = chunk_max_bytes(g, last_tok * g.HD / d.V);
+    *bytes = g.n_planes * ((g.P - 1) * full + last);
+    return SKV_OK;
+}
+
+int32_t skv_workspace_bytes(const skv_layout *lay, int32_t encode, uint64_t *bytes) {
+    Geom g;
+    if (make_geom(lay, g) != SKV_OK || !bytes) return SKV_ERR_INVALID_ARG;
+    *bytes = carve(g, encode != 0, nullptr).bytes;
+    return SKV_OK;
+}
+
+int32_t skv_encode(const skv_layout *lay, const void *kv, const void *mu, const float *sigma,
+                   const uint64_t *counts, void *out, uint64_t out_capacity, uint64_t *offsets,
+                   int32_t *status, void *workspace, uint64_t ws_bytes, void *stream) {
+    Geom g;
+    int32_t r = make_geom(lay, g);
+    if (r != SKV_OK) return r;
+    r = common_checks(g, sigma, counts, status, workspace, ws_bytes, true);
+    if (r != SKV_OK) return r;
+    if (!offsets || (g.n_chunks && (!kv || !mu || !out))) return SKV_ERR_INVALID_ARG;
+    if (g.n_chunks && (!aligned16(kv) || !aligned16(mu) || !aligned16(out))) return SKV_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return SKV_ERR_CUDA;
+    const Workspace ws = carve(g, true, static_cast<uint8_t *>(workspace));
+    if ((r = run_setup(g, sigma, counts, ws, status, st)) != SKV_OK) return r;
+    EncArgs ea{g, static_cast<const uint8_t *>(kv), static_cast<const uint8_t *>(mu), ws.phat,
+               ws.rsig, ws.states, ws.nwords, ws.scratch, status};
+    if (launch_encode(ea, st)) return SKV_ERR_CUDA;
+    ScanArgs sa{g, ws.nwords, offsets, out_capacity, status};
+    if (launch_scan(sa, st)) return SKV_ERR_CUDA;
+    CompactArgs ca{g, ws.states, ws.nwords, ws.scratch, offsets, static_cast<uint8_t *>(out),
+                   out_capacity};
+    if (launch_compact(ca, st)) return SKV_ERR_CUDA;
+    return SKV_OK;
+}
+
+static int32_t decode_impl(const skv_layout *lay, const void *bitstream, uint64_t bitstream_bytes,
+                           const uint64_t *offsets, const void *mu, const float *sigma,
+                           const uint64_t *counts, const uint32_t *ids, uint64_t n_units,
+                           bool pages, void *out, int32_t *status, void *workspace,
+                           uint64_t ws_bytes, void *stream) {
+    Geom g;
+    int32_t r = make_geom(lay, g);
+    if (r != SKV_OK) return r;
+    r = common_checks(g, sigma, counts, status, workspace, ws_bytes, false);
+    if (r != SKV_OK) return r;
+    if (!pages) n_units = g.n_chunks;
+    if (n_units && (!bitstream || !offsets || !mu || !out)) return SKV_ERR_INVALID_ARG;
+    if (pages && n_units && !ids) return SKV_ERR_INVALID_ARG;
+    if (n_units && (!aligned16(bitstream) || !aligned16(mu) || !aligned16(out))) return SKV_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return SKV_ERR_CUDA;
+    const Workspace ws = carve(g, false, static_cast<uint8_t *>(workspace));
+    if ((r = run_setup(g, sigma, counts, ws, status, st)) != SKV_OK) return r;
+    DecArgs da{g, static_cast<const uint8_t *>(bitstream), bitstream_bytes, offsets,
+               static_cast<const uint8_t *>(mu), ws.phat, ws.rsig, pages ? ids : nullptr,
+               n_units, static_cast<uint8_t *>(out), (uint64_t)g.Tc * g.HD, status};
+    if (launch_decode(da, st)) return SKV_ERR_CUDA;
+    return SKV_OK;
+}
+
+int32_t skv_decode(const skv_layout *lay, const void *bitstream, uint64_t bitstream_bytes,
+                   const uint64_t *offsets, const void *mu, const float *sigma,
+                   const uint64_t *counts, void *kv_out, int32_t *status, void *workspace,
+                   uint64_t ws_bytes, void *stream) {
+    return decode_impl(lay, bitstream, bitstream_bytes, offsets, mu, sigma, counts, nullptr, 0,
+                       false, kv_out, status, workspace, ws_bytes, stream);
+}
+
+int32_t skv_decode_chunks(const skv_layout *lay, const void *bitstream, uint64_t bitstream_bytes,
+                          const uint64_t *offsets, const void *mu, const float *sigma,
+                          const uint64_t *counts, const uint32_t *chunk_ids, uint32_t n_ids,
+                          void *pages_out, int32_t *status, void *workspace, uint64_t ws_bytes,
+                          void *stream) {
+    return decode_impl(lay, bitstream, bitstream_bytes, offsets, mu, sigma, counts, chunk_ids,
+                       n_ids, true, pages_out, status, workspace, ws_bytes, stream);
+}
+
+int32_t skv_cdf_eval(const skv_layout *lay, const uint64_t *counts, uint64_t n,
+                     const uint32_t *mu_codes, const float *sigmas, const uint32_t *ords,
+                     uint32_t *C_out, int32_t *status, void *workspace, uint64_t ws_bytes,
+                     void *stream) {
+    Geom g;
+    int32_t r = make_geom(lay, g);
+    if (r != SKV_OK) return r;
+    if (!status || !workspace || (g.w_h && !counts)) return SKV_ERR_INVALID_ARG;
+    if (n && (!mu_codes || !sigmas || !ords || !C_out)) return SKV_ERR_INVALID_ARG;
+    if (((uintptr_t)workspace & 255u) != 0 || ws_bytes < carve(g, false, nullptr).bytes)
+        return SKV_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return SKV_ERR_CUDA;
+    const Workspace ws = carve(g, false, static_cast<uint8_t *>(workspace));
+    // P_hat only; sigma is per query here, so rsig is not built
+    Geom g1 = g;
+    g1.n_planes = 0;
+    SetupArgs s{g1, nullptr, counts, ws.phat, ws.rsig, status};
+    if (g.dtype == SKV_BF16) setup_kernel<SKV_BF16><<<1, 1024, 0, st>>>(s);
+    else setup_kernel<SKV_E4M3><<<1, 1024, 0, st>>>(s);
+    if (cudaGetLastError() != cudaSuccess) return SKV_ERR_CUDA;
+    if (n == 0) return SKV_OK;
+    CdfArgs ca{g, ws.phat, n, mu_codes, sigmas, ords, C_out, status};
+    const uint64_t blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+    if (g.dtype == SKV_BF16) cdf_eval_kernel<SKV_BF16><<<(unsigned)blocks, 256, 0, st>>>(ca);
+    else cdf_eval_kernel<SKV_E4M3><<<(unsigned)blocks, 256, 0, st>>>(ca);
+    return cudaGetLastError() == cudaSuccess ? SKV_OK : SKV_ERR_CUDA;
+}
+
+}  // extern "C"

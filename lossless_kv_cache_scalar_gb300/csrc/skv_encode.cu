@@ -1,0 +1,201 @@
+// skv_encode.cu -- encoder kernels: per-scalar model + warp-interleaved rANS,
+// chunk-size scan, and compaction into the final bitstream (FORMAT.md 6-7).
+//
+// The encoder is the "arithmetic coder emits bits" box of the Speculative KV
+// Coding wiki's pipeline section, in its rANS form. One warp owns one group of
+// 32 streams of one chunk; lane l is stream 32 g + l. A stream is encoded
+// backwards (rANS is last-in first-out), so the warp walks its vectors from
+// the last to the first and each vector's scalars from the last to the first.
+// The words a step emits are ordered with a ballot: the decoder will read them
+// at that step in ascending lane order, so the encoder writes them, downwards
+// from the top of the group's scratch slot, in the same ascending order.
+#include <cuda_runtime.h>
+
+#include "skv_model.cuh"
+
+namespace skv {
+
+constexpr int kEncWarps = 8;
+
+template <uint32_t DT>
+__global__ void __launch_bounds__(kEncWarps * 32, 3) encode_kernel(const EncArgs a) {
+    using K = Codes<DT>;
+    constexpr uint32_t V = K::V;
+    __shared__ Tables tab;
+    __shared__ Tables8 tab8;
+    stage_tables<DT>(tab, tab8, a.phat);
+
+    const Geom &g = a.g;
+    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+    const uint64_t gid = (uint64_t)blockIdx.x * kEncWarps + warp;
+    if (gid >= g.n_groups) return;
+    const uint64_t k = gid / g.G;
+    const uint32_t grp = (uint32_t)(gid % g.G);
+    const ChunkSpan cs = chunk_span(g, k);
+    const uint32_t s = grp * 32u + lane;
+    const int64_t nq = (int64_t)stream_vectors(g, cs.n_vec, s);
+    const int64_t nq0 = (int64_t)stream_vectors(g, cs.n_vec, grp * 32u);
+    const uint8_t *kvp = a.kv + cs.elem0 * K::bytes;
+    const uint8_t *mup = a.mu + cs.elem0 * K::bytes;
+    const float *rsp = a.rsig + cs.plane * g.HD;
+    uint32_t *slot = a.scratch + gid * g.cap_words;
+    const Weights w{g.w_n, g.w_w, g.w_h};
+    const uint32_t lt = lanemask_lt();
+
+    int64_t pos = (int64_t)g.cap_words;   // words live in [pos, cap_words)
+    uint64_t x = K::L;
+    bool bad_mu = false, overflow = false;
+
+    // Register double buffer: the next vector is in flight while one is coded.
+    uint4 kv_n = make_uint4(0, 0, 0, 0), mu_n = kv_n;
+    float4 rs_n[V / 4];
+    auto fetch = [&](int64_t j) {
+        if (j >= 0 && j < nq) {
+            const uint64_t q = s + (uint64_t)j * g.W;
+            kv_n = __ldg(reinterpret_cast<const uint4 *>(kvp) + q);
+            mu_n = __ldg(reinterpret_cast<const uint4 *>(mup) + q);
+            const uint32_t c0 = (uint32_t)((q * V) % g.HD);
+#pragma unroll
+            for (int i = 0; i < (int)(V / 4); ++i)
+                rs_n[i] = __ldg(reinterpret_cast<const float4 *>(rsp + c0) + i);
+        }
+    };
+    fetch(nq0 - 1);
+
+    for (int64_t j = nq0 - 1; j >= 0; --j) {
+        const bool active = j < nq;
+        const uint4 kvv = kv_n, muv = mu_n;
+        float rsv[V];
+#pragma unroll
+        for (int i = 0; i < (int)(V / 4); ++i) {
+            rsv[4 * i + 0] = rs_n[i].x; rsv[4 * i + 1] = rs_n[i].y;
+            rsv[4 * i + 2] = rs_n[i].z; rsv[4 * i + 3] = rs_n[i].w;
+        }
+        fetch(j - 1);
+#pragma unroll
+        for (int e = (int)V - 1; e >= 0; --e) {
+            uint32_t c = 0, f = 1;
+            if (active) {
+                const uint32_t mc = K::get(muv, e);
+                const bool fin = K::finite(mc);
+                bad_mu |= !fin;
+                const float mu = fin ? K::value(mc) : 0.0f;
+                const uint32_t o = K::ord(K::get(kvv, e));
+                c = cdf<DT>(tab, &tab8, w, a.phat, o, mu, rsv[e]);
+                f = cdf<DT>(tab, &tab8, w, a.phat, o + 1u, mu, rsv[e]) - c;
+            }
+            const bool emit = active && (x >= ((uint64_t)f << 39));
+            const uint32_t ball = __ballot_sync(0xFFFFFFFFu, emit);
+            if (ball) {
+                const int cnt = __popc(ball);
+                if (emit) {
+                    const int64_t idx = pos - cnt + __popc(ball & lt);
+                    if (idx >= 0) slot[idx] = (uint32_t)x;
+                    else overflow = true;
+                    x >>= 32;
+                }
+                pos -= cnt;
+            }
+            if (active) x = rans_put<DT>(x, c, f);
+        }
+    }
+    a.states[gid * 32u + lane] = x;
+    if (lane == 0) a.nwords[gid] = pos >= 0 ? (uint32_t)(g.cap_words - pos) : 0u;
+    if (__any_sync(0xFFFFFFFFu, bad_mu) && lane == 0) set_status(a.status, SKV_ERR_NONFINITE_MU);
+    if (__any_sync(0xFFFFFFFFu, overflow) && lane == 0) set_status(a.status, SKV_ERR_CAPACITY);
+}
+
+// Per-chunk sizes (FORMAT.md section 7) and their exclusive scan into offsets.
+__global__ void __launch_bounds__(1024) scan_kernel(const ScanArgs a) {
+    const Geom &g = a.g;
+    __shared__ uint64_t warp_tot[32];
+    __shared__ uint64_t carry;
+    const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (uint64_t base = 0; base < g.n_chunks; base += 1024) {
+        const uint64_t k = base + tid;
+        uint64_t size = 0;
+        if (k < g.n_chunks) {
+            size = g.hdr_bytes;
+            for (uint32_t j = 0; j < g.G; ++j) size += pad16(4ull * a.nwords[k * g.G + j]);
+        }
+        uint64_t incl = size;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint64_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+            if (lane >= (uint32_t)d) incl += v;
+        }
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            uint64_t t = warp_tot[lane];
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const uint64_t v = __shfl_up_sync(0xFFFFFFFFu, t, d);
+                if (lane >= (uint32_t)d) t += v;
+            }
+            warp_tot[lane] = t;
+        }
+        __syncthreads();
+        const uint64_t before = carry + (warp ? warp_tot[warp - 1] : 0ull) + incl - size;
+        if (k < g.n_chunks) a.offsets[k] = before;
+        __syncthreads();
+        if (tid == 1023) carry = before + size;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        a.offsets[g.n_chunks] = carry;
+        if (carry > a.out_capacity) set_status(a.status, SKV_ERR_CAPACITY);
+    }
+}
+
+// Copy each chunk's states, word counts and words to its place in the stream.
+__global__ void __launch_bounds__(256) compact_kernel(const CompactArgs a) {
+    const Geom &g = a.g;
+    for (uint64_t k = blockIdx.x; k < g.n_chunks; k += gridDim.x) {
+        const uint64_t off = a.offsets[k], end = a.offsets[k + 1];
+        if (end > a.out_capacity) continue;
+        uint8_t *dst = a.out + off;
+        uint64_t *st = reinterpret_cast<uint64_t *>(dst);
+        for (uint32_t i = threadIdx.x; i < g.W; i += blockDim.x) st[i] = a.states[k * g.W + i];
+        uint32_t *hw = reinterpret_cast<uint32_t *>(dst + 8ull * g.W);
+        const uint32_t hwords = (uint32_t)(pad16(4ull * g.G) / 4);
+        for (uint32_t i = threadIdx.x; i < hwords; i += blockDim.x)
+            hw[i] = i < g.G ? a.nwords[k * g.G + i] : 0u;
+        uint64_t pos = g.hdr_bytes;
+        for (uint32_t j = 0; j < g.G; ++j) {
+            const uint64_t gid = k * g.G + j;
+            const uint32_t nw = a.nwords[gid];
+            const uint32_t *src = a.scratch + gid * g.cap_words + (g.cap_words - nw);
+            uint32_t *dw = reinterpret_cast<uint32_t *>(dst + pos);
+            const uint32_t padded = (nw + 3u) & ~3u;
+            for (uint32_t i = threadIdx.x; i < padded; i += blockDim.x) dw[i] = i < nw ? src[i] : 0u;
+            pos += 4ull * padded;
+        }
+    }
+}
+
+int launch_encode(const EncArgs &a, cudaStream_t st) {
+    const uint64_t blocks = (a.g.n_groups + kEncWarps - 1) / kEncWarps;
+    if (blocks == 0) return 0;
+    if (a.g.dtype == SKV_BF16)
+        encode_kernel<SKV_BF16><<<(unsigned)blocks, kEncWarps * 32, 0, st>>>(a);
+    else
+        encode_kernel<SKV_E4M3><<<(unsigned)blocks, kEncWarps * 32, 0, st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? 0 : 1;
+}
+
+int launch_scan(const ScanArgs &a, cudaStream_t st) {
+    scan_kernel<<<1, 1024, 0, st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? 0 : 1;
+}
+
+int launch_compact(const CompactArgs &a, cudaStream_t st) {
+    if (a.g.n_chunks == 0) return 0;
+    const uint64_t blocks = a.g.n_chunks < 65535u ? a.g.n_chunks : 65535u;
+    compact_kernel<<<(unsigned)blocks, 256, 0, st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? 0 : 1;
+}
+
+}  // namespace skv

@@ -1,0 +1,136 @@
+// skv_internal.h -- host/device shared geometry and kernel argument blocks.
+//
+// Geometry follows FORMAT.md section 7: a chunk is one (layer, kv, page of
+// tokens_per_chunk tokens) block, contiguous in the canonical layout; it has
+// G = W/32 groups of 32 interleaved rANS streams; stream s = 32 g + lane owns
+// the 16-byte vectors q with q mod W == s.
+#pragma once
+
+#include <cstdint>
+
+#include "../../include/skv.h"
+
+#define SKV_HD __host__ __device__ __forceinline__
+
+namespace skv {
+
+struct DtypeInfo {
+    uint32_t N;       // codes
+    uint32_t m;       // log2 of the total frequency M
+    uint32_t V;       // codes per 16-byte vector
+    uint32_t bytes;   // bytes per code
+};
+
+SKV_HD DtypeInfo dtype_info(uint32_t dtype) {
+    DtypeInfo d;
+    if (dtype == SKV_BF16) { d.N = 65536u; d.m = 24u; d.V = 8u; d.bytes = 2u; }
+    else                   { d.N = 256u;   d.m = 16u; d.V = 16u; d.bytes = 1u; }
+    return d;
+}
+
+// Everything a kernel needs to walk chunks and streams, precomputed on the host.
+struct Geom {
+    uint32_t dtype;
+    uint32_t n_kv, HD, W, G, Tc;
+    uint64_t T;            // tokens per plane
+    uint64_t P;            // pages per plane
+    uint64_t n_chunks;
+    uint64_t n_groups;     // n_chunks * G
+    uint64_t n_planes;     // n_layers * n_kv
+    uint32_t w_n, w_w, w_h;
+    uint32_t hdr_bytes;    // 8 W + pad16(4 G)
+    uint64_t cap_words;    // scratch words per group (encoder)
+};
+
+SKV_HD uint64_t pad16(uint64_t b) { return (b + 15u) & ~uint64_t(15); }
+
+// Chunk k: its plane, its first global element, and its vector count.
+struct ChunkSpan {
+    uint64_t plane;
+    uint64_t elem0;
+    uint64_t n_vec;
+};
+
+SKV_HD ChunkSpan chunk_span(const Geom &g, uint64_t k) {
+    ChunkSpan c;
+    uint64_t page = k % g.P;
+    c.plane = k / g.P;
+    uint64_t tok0 = page * g.Tc;
+    uint64_t ntok = g.T - tok0;
+    if (ntok > g.Tc) ntok = g.Tc;
+    c.elem0 = (c.plane * g.T + tok0) * g.HD;
+    c.n_vec = ntok * g.HD / dtype_info(g.dtype).V;
+    return c;
+}
+
+// Number of vectors owned by stream s of a chunk with n_vec vectors.
+SKV_HD uint64_t stream_vectors(const Geom &g, uint64_t n_vec, uint32_t s) {
+    return n_vec > s ? (n_vec - s + g.W - 1) / g.W : 0;
+}
+
+struct SetupArgs {
+    Geom g;
+    const float *sigma;
+    const uint64_t *counts;
+    uint32_t *phat;        // N + 1 entries
+    float *rsig;           // n_planes * HD
+    int32_t *status;
+};
+
+struct EncArgs {
+    Geom g;
+    const uint8_t *kv;
+    const uint8_t *mu;
+    const uint32_t *phat;
+    const float *rsig;
+    uint64_t *states;      // n_groups * 32
+    uint32_t *nwords;      // n_groups
+    uint32_t *scratch;     // n_groups * cap_words
+    int32_t *status;
+};
+
+struct ScanArgs {
+    Geom g;
+    const uint32_t *nwords;
+    uint64_t *offsets;     // n_chunks + 1
+    uint64_t out_capacity;
+    int32_t *status;
+};
+
+struct CompactArgs {
+    Geom g;
+    const uint64_t *states;
+    const uint32_t *nwords;
+    const uint32_t *scratch;
+    const uint64_t *offsets;
+    uint8_t *out;
+    uint64_t out_capacity;
+};
+
+struct DecArgs {
+    Geom g;
+    const uint8_t *stream;
+    uint64_t stream_bytes;
+    const uint64_t *offsets;
+    const uint8_t *mu;
+    const uint32_t *phat;
+    const float *rsig;
+    const uint32_t *ids;   // NULL: all chunks in order; else chunk ids (page mode)
+    uint64_t n_units;      // chunks to decode (n_chunks or n_ids)
+    uint8_t *out;          // canonical layout, or pages of page_elems codes
+    uint64_t page_elems;
+    int32_t *status;
+};
+
+struct CdfArgs {
+    Geom g;
+    const uint32_t *phat;
+    uint64_t n;
+    const uint32_t *mu_codes;
+    const float *sigmas;
+    const uint32_t *ords;
+    uint32_t *C;
+    int32_t *status;
+};
+
+}  // namespace skv

@@ -1,0 +1,210 @@
+// skv_model.cuh -- the per-scalar mixture model and the rANS step, on the device.
+//
+// The model is the three-component mixture of the Speculative KV Coding wiki
+// (mixture section): 0.95 N(mu, sigma^2) + 0.03 N(mu, (3 sigma)^2) +
+// 0.02 p_hat, integrated over each code's rounding interval. Its integer form
+// (FORMAT.md section 5) must be bit-identical at encoder and decoder, which
+// the 推测性KV编码 blog's deployment section demands of any arithmetic coder:
+// every float step below is one IEEE binary32 operation with round-to-nearest,
+// written with explicit _rn intrinsics so nothing is contracted into an FMA,
+// and the build keeps subnormals (no -ftz).
+#pragma once
+
+#include <cstdint>
+
+#include "phi_q24.h"
+#include "skv_internal.h"
+
+namespace skv {
+
+// T[j + 2048] = round_half_even(2^24 Phi(j / 256)), FORMAT.md section 3.
+static __device__ const uint32_t kPhiQ24[4097] = {SKV_PHI_Q24_VALUES};
+
+// Tables staged in shared memory by every CTA that evaluates the model.
+struct Tables {
+    uint2 phi[4097];     // (T[j], T[j+1] - T[j]); entry 4096 = (2^24, 0)
+};
+struct Tables8 {         // e4m3 only: the whole alphabet fits on chip
+    float edge[257];
+    uint32_t phat[257];
+};
+
+struct Weights {
+    uint32_t n, w, h;    // narrow, wide, marginal; sum 100
+};
+
+// ---------------------------------------------------------------- code order
+
+template <uint32_t DT> struct Codes;
+
+template <> struct Codes<SKV_BF16> {
+    static constexpr uint32_t N = 65536u, m = 24u, V = 8u, bytes = 2u;
+    static constexpr uint64_t L = 1ull << 31;
+    __device__ __forceinline__ static uint32_t ord(uint32_t b) {
+        return b ^ ((b & 0x8000u) ? 0xFFFFu : 0x8000u);
+    }
+    __device__ __forceinline__ static uint32_t code(uint32_t o) {
+        return o ^ ((o < 0x8000u) ? 0xFFFFu : 0x8000u);
+    }
+    __device__ __forceinline__ static bool finite(uint32_t b) { return (b & 0x7F80u) != 0x7F80u; }
+    __device__ __forceinline__ static float value(uint32_t b) { return __uint_as_float(b << 16); }
+    // Edge E(o) (FORMAT.md section 2) straight from the bits: for a positive code
+    // k >= 1 the binary32 pattern (k << 16) - 0x8000 lies half a bf16 step below
+    // code k, which is the exact midpoint of codes k-1 and k (binary32 spacing is
+    // uniform within a binade and the bf16 grid is a subset of it); negative
+    // edges mirror positive ones, E(o) = -E(N - o).
+    __device__ __forceinline__ static float edge(const Tables8 *, uint32_t o) {
+        const int k = (int)o - 32768;
+        const uint32_t a = (uint32_t)abs(k);
+        uint32_t bits = (a << 16) - 0x8000u;
+        bits = (a == 0u) ? 0u : bits;
+        bits = (a > 0x7F7Fu) ? 0x7F800000u : bits;
+        bits |= (k < 0) ? 0x80000000u : 0u;
+        return __uint_as_float(bits);
+    }
+    __device__ __forceinline__ static uint32_t phat(const Tables8 *, const uint32_t *__restrict__ g,
+                                                    uint32_t o) {
+        return __ldg(g + o);
+    }
+    // element e of a 16-byte vector
+    __device__ __forceinline__ static uint32_t get(const uint4 &v, int e) {
+        const uint32_t w = (e >> 1) == 0 ? v.x : (e >> 1) == 1 ? v.y : (e >> 1) == 2 ? v.z : v.w;
+        return (e & 1) ? (w >> 16) : (w & 0xFFFFu);
+    }
+    __device__ __forceinline__ static void put(uint4 &v, int e, uint32_t c) {
+        uint32_t &w = (e >> 1) == 0 ? v.x : (e >> 1) == 1 ? v.y : (e >> 1) == 2 ? v.z : v.w;
+        w = (e & 1) ? ((w & 0xFFFFu) | (c << 16)) : ((w & 0xFFFF0000u) | c);
+    }
+};
+
+template <> struct Codes<SKV_E4M3> {
+    static constexpr uint32_t N = 256u, m = 16u, V = 16u, bytes = 1u;
+    static constexpr uint64_t L = 1ull << 23;
+    __device__ __forceinline__ static uint32_t ord(uint32_t b) {
+        return b ^ ((b & 0x80u) ? 0xFFu : 0x80u);
+    }
+    __device__ __forceinline__ static uint32_t code(uint32_t o) {
+        return o ^ ((o < 0x80u) ? 0xFFu : 0x80u);
+    }
+    __device__ __forceinline__ static bool finite(uint32_t b) { return (b & 0x7Fu) != 0x7Fu; }
+    // OCP e4m3: bias 7, 3 mantissa bits, subnormals m * 2^-9, no infinity.
+    __device__ __forceinline__ static float value(uint32_t b) {
+        const uint32_t e = (b >> 3) & 15u, mt = b & 7u;
+        float v = (e == 0u) ? __fmul_rn(__uint2float_rn(mt), 0.001953125f)
+                            : __uint_as_float(((e + 120u) << 23) | (mt << 20));
+        return (b & 0x80u) ? -v : v;
+    }
+    __device__ __forceinline__ static float edge(const Tables8 *t8, uint32_t o) { return t8->edge[o]; }
+    __device__ __forceinline__ static uint32_t phat(const Tables8 *t8, const uint32_t *, uint32_t o) {
+        return t8->phat[o];
+    }
+    __device__ __forceinline__ static uint32_t get(const uint4 &v, int e) {
+        const uint32_t w = (e >> 2) == 0 ? v.x : (e >> 2) == 1 ? v.y : (e >> 2) == 2 ? v.z : v.w;
+        return (w >> (8 * (e & 3))) & 0xFFu;
+    }
+    __device__ __forceinline__ static void put(uint4 &v, int e, uint32_t c) {
+        uint32_t &w = (e >> 2) == 0 ? v.x : (e >> 2) == 1 ? v.y : (e >> 2) == 2 ? v.z : v.w;
+        const int sh = 8 * (e & 3);
+        w = (w & ~(0xFFu << sh)) | (c << sh);
+    }
+};
+
+// Edge of ordinal o computed from the code values (FORMAT.md section 2), used to
+// fill the e4m3 edge table; the bf16 path uses the equivalent bit form above.
+template <uint32_t DT>
+__device__ float edge_from_values(uint32_t o) {
+    using K = Codes<DT>;
+    const uint32_t maxc = (DT == SKV_BF16) ? 0x7F7Fu : 0x7Eu;
+    const uint32_t o_lo = K::ord(maxc | (K::N / 2)), o_hi = K::ord(maxc);
+    if (o <= o_lo) return __int_as_float(0xFF800000);
+    if (o > o_hi) return __int_as_float(0x7F800000);
+    const float a = K::value(K::code(o - 1)), b = K::value(K::code(o));
+    return __fadd_rn(__fmul_rn(0.5f, a), __fmul_rn(0.5f, b));
+}
+
+// Stage the Phi pairs (and, for e4m3, the edges and P_hat) into shared memory.
+template <uint32_t DT>
+__device__ void stage_tables(Tables &t, Tables8 &t8, const uint32_t *__restrict__ phat) {
+    for (uint32_t i = threadIdx.x; i < 4097u; i += blockDim.x) {
+        const uint32_t a = kPhiQ24[i];
+        const uint32_t b = (i < 4096u) ? kPhiQ24[i + 1] : a;
+        t.phi[i] = make_uint2(a, b - a);
+    }
+    if (DT == SKV_E4M3) {
+        for (uint32_t o = threadIdx.x; o <= 256u; o += blockDim.x) {
+            t8.edge[o] = edge_from_values<SKV_E4M3>(o);
+            t8.phat[o] = phat[o];
+        }
+    }
+    __syncthreads();
+}
+
+// -------------------------------------------------------------- model: C(o)
+
+// Phi_q(zq) for zq already clamped to [-2^19, 2^19] (FORMAT.md section 3).
+__device__ __forceinline__ uint32_t phi_q(const uint2 *__restrict__ tab, int zq) {
+    const uint2 e = tab[(zq >> 8) + 2048];
+    return e.x + ((e.y * (uint32_t)(zq & 255)) >> 8);
+}
+
+// C(o) for an element with predictor value mu and rs = fl32(1/sigma).
+template <uint32_t DT>
+__device__ __forceinline__ uint32_t cdf(const Tables &t, const Tables8 *t8, const Weights w,
+                                        const uint32_t *__restrict__ phat, uint32_t o, float mu,
+                                        float rs) {
+    using K = Codes<DT>;
+    constexpr uint32_t MN = (1u << K::m) - K::N;
+    const float E = K::edge(t8, o);
+    const float d = __fsub_rn(E, mu);
+    float z = __fmul_rn(d, rs);
+    z = fminf(fmaxf(z, -24.0f), 24.0f);
+    const int zq = __float2int_rd(__fmul_rn(z, 65536.0f));
+    const int zn = max(min(zq, 524288), -524288);
+    uint32_t S = w.n * phi_q(t.phi, zn);
+    if (w.w) {
+        // floor(zq / 3) for zq in [-3 * 2^19, 3 * 2^19]
+        const int zw = (int)(__umulhi((uint32_t)(zq + 1572864), 0xAAAAAAABu) >> 1) - 524288;
+        S += w.w * phi_q(t.phi, zw);
+    }
+    if (w.h) S += w.h * K::phat(t8, phat, o);
+    const uint64_t prod = (uint64_t)S * MN;
+    return o + (uint32_t)(prod >> 24) / 100u;
+}
+
+// ------------------------------------------------------------------- rANS
+
+// q = floor(x / f), r = x mod f for f in [1, 2^24] and x < 2^39 f.
+// A binary32 reciprocal estimate gives q to within 2^17 + 1; one more estimate
+// on the signed remainder lands within one step, fixed by a final compare.
+__device__ __forceinline__ uint64_t divmod(uint64_t x, uint32_t f, uint32_t &r_out) {
+    float rf;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rf) : "f"(__uint2float_rn(f)));
+    const uint64_t q1 = __float2ull_rz(__fmul_rn(__ull2float_rn(x), rf));
+    long long r = (long long)(x - q1 * (uint64_t)f);
+    const int q2 = __float2int_rn(__fmul_rn(__ll2float_rn(r), rf));
+    r -= (long long)q2 * (long long)f;
+    long long q = (long long)q1 + q2;
+    if (r < 0) { r += f; q -= 1; }
+    r_out = (uint32_t)r;
+    return (uint64_t)q;
+}
+
+// Encode one symbol after renormalisation: x = (x / f) M + (x mod f) + c.
+template <uint32_t DT>
+__device__ __forceinline__ uint64_t rans_put(uint64_t x, uint32_t c, uint32_t f) {
+    uint32_t r;
+    const uint64_t q = divmod(x, f, r);
+    return (q << Codes<DT>::m) + r + c;
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+__device__ __forceinline__ void set_status(int32_t *status, int32_t code) {
+    atomicCAS(status, 0, code);
+}
+
+}  // namespace skv

@@ -1,0 +1,288 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+The bar is bit-exactness everywhere: the model's cumulative frequencies, the
+compressed bitstream and offsets, and the decoded KV codes. Inputs are the
+seeded synthetic workloads (same recipe as the benchmark) at sizes the oracle
+finishes in seconds, spanning several chunks and a ragged tail; the
+full-size workloads are checked on sampled chunks (bytes equal to the
+oracle's encoding of that chunk alone) and by exact round trip.
+"""
+import numpy as np
+import pytest
+import torch
+
+from lossless_kv_cache_scalar_gb300 import Coder, Layout, SKVError, cdf_eval, synth
+from oracle import oracle as O
+from tests import _skvtest as H
+
+pytestmark = pytest.mark.gpu
+
+
+def _bf16(x):
+    return int(torch.tensor([x]).to(torch.bfloat16).view(torch.int16).item()) & 0xFFFF
+
+
+def _e4m3(x):
+    return int(torch.tensor([x]).to(torch.float8_e4m3fn).view(torch.uint8).item())
+
+
+# ---------------------------------------------------------------- the model
+
+MODEL_CASES = {
+    "bf16": [(1.5, 2.0 ** -5), (-0.0731, 0.004), (0.0, 1e-3), (3.0e-39, 1e-36), (-3.3e38, 1e37),
+             (12.5, 2.0 ** -126), (0.25, 1e30), (7.0, 0.031), (-2.0e-3, 50.0), (1e-40, 3.0)],
+    "e4m3": [(1.0, 0.4), (-37.0, 3.0), (0.0, 0.02), (448.0, 100.0), (-0.015625, 2.0 ** -126),
+             (3.0, 1e30)],
+}
+
+
+@pytest.mark.parametrize("dt", ["bf16", "e4m3"])
+@pytest.mark.parametrize("weights", [(95, 3, 2), (100, 0, 0), (0, 0, 100), (50, 30, 20)])
+def test_cdf_kernel_all_ordinals(dt, weights):
+    n = 65536 if dt == "bf16" else 256
+    rng = np.random.default_rng(17)
+    counts = rng.integers(0, 40, n).astype(np.uint64)
+    counts[rng.integers(0, n, n // 3)] = 0
+    mus, sigs, ords = [], [], []
+    for mu, sg in MODEL_CASES[dt]:
+        mc = _bf16(mu) if dt == "bf16" else _e4m3(mu)
+        mus.append(np.full(n + 1, mc, np.uint32))
+        sigs.append(np.full(n + 1, sg, np.float32))
+        ords.append(np.arange(n + 1, dtype=np.uint32))
+    # plus random (mu code, sigma) pairs over the whole finite range
+    k = 20000
+    rmu = rng.integers(0, n, k).astype(np.uint32)
+    fin = (rmu & 0x7F80) != 0x7F80 if dt == "bf16" else (rmu & 0x7F) != 0x7F
+    rmu[~fin] = 0
+    mus.append(rmu)
+    sigs.append(np.exp(rng.uniform(-80, 80, k)).astype(np.float32).clip(2.0 ** -126, 3e38))
+    ords.append(rng.integers(0, n + 1, k).astype(np.uint32))
+    mus, sigs, ords = (np.concatenate(a) for a in (mus, sigs, ords))
+    want = O.cdf_eval(O.BF16 if dt == "bf16" else O.E4M3, mus, sigs, ords, weights, counts)
+    lay = Layout(dt, 1, 1, 1, 16, 1, weights=weights)
+    t = lambda a, d: torch.from_numpy(a.view(d)).cuda()  # noqa: E731
+    got = cdf_eval(lay, t(counts, np.int64), t(mus, np.int32), t(sigs, np.float32), t(ords, np.int32))
+    got = got.cpu().numpy().astype(np.uint64)
+    bad = np.flatnonzero(got != want)
+    assert bad.size == 0, (bad[:5], got[bad[:5]], want[bad[:5]], mus[bad[:5]], sigs[bad[:5]], ords[bad[:5]])
+
+
+# ------------------------------------------------------------- whole streams
+
+def _workload(cfg):
+    w = synth.generate(cfg)
+    return H.dev(w), H.host(w)
+
+
+def test_tiny_bitexact():
+    cfg = synth.CONFIGS["tiny"]
+    wd, wh = _workload(cfg)
+    H.assert_same_stream(H.layout_of(cfg), wd, wh)
+
+
+SCALED = [
+    ("qwen3_0p6b", dict(n_layers=2, n_tokens=1024 + 37)),
+    ("qwen3_8b", dict(n_layers=1, n_tokens=1100)),
+    ("fp8_32b", dict(n_layers=2, n_tokens=600, calib_tokens=512)),
+    ("paged_14b", dict(n_layers=1, n_tokens=700, calib_tokens=512)),
+]
+
+
+@pytest.mark.parametrize("name,kw", SCALED, ids=[s[0] for s in SCALED])
+def test_config_recipes_bitexact(name, kw):
+    cfg = synth.CONFIGS[name].scaled(**kw)
+    wd, wh = _workload(cfg)
+    H.assert_same_stream(H.layout_of(cfg), wd, wh)
+
+
+@pytest.mark.parametrize("W,Tc,T", [(32, 256, 300), (96, 100, 257), (256, 7, 20), (128, 1, 3),
+                                    (64, 256, 1), (32, 64, 130)])
+def test_geometries_bitexact(W, Tc, T):
+    cfg = synth.CONFIGS["tiny"].scaled(n_tokens=T, n_heads=2, head_dim=64, seed=300 + W + T)
+    wd, wh = _workload(cfg)
+    H.assert_same_stream(H.layout_of(cfg, tokens_per_chunk=Tc, streams_per_chunk=W), wd, wh)
+
+
+def test_empty_input():
+    lay = Layout("bf16", 2, 2, 8, 128, 0)
+    c = Coder(lay)
+    z = torch.empty((2, 2, 0, 8, 128), dtype=torch.int16, device="cuda")
+    sig = torch.ones((2, 2, 8, 128), device="cuda")
+    cnt = torch.ones(65536, dtype=torch.int64, device="cuda")
+    s, offs = c.encode(z, z, sig, cnt)
+    assert s.numel() == 0 and offs.numel() == 1 and int(offs[0]) == 0
+    back = c.decode(s, offs, z, sig, cnt)
+    assert back.numel() == 0
+
+
+@pytest.mark.parametrize("weights", [(100, 0, 0), (0, 0, 100), (50, 30, 20), (0, 100, 0)])
+def test_weights_bitexact(weights):
+    cfg = synth.CONFIGS["tiny"].scaled(n_tokens=300, seed=55)
+    wd, wh = _workload(cfg)
+    H.assert_same_stream(H.layout_of(cfg, weights=weights), wd, wh)
+
+
+def test_all_bf16_bit_patterns():
+    rng = np.random.default_rng(9)
+    lay = Layout("bf16", 1, 1, 1, 1024, 80)
+    n = lay.n_elems
+    kv = rng.integers(0, 65536, n).astype(np.uint16)
+    kv[:65536] = np.arange(65536, dtype=np.uint16)
+    mu = rng.integers(0, 65536, n).astype(np.uint16)
+    mu[(mu & 0x7F80) == 0x7F80] = 0x3F80
+    sigma = np.exp(rng.normal(0, 4, 1024)).astype(np.float32)
+    counts = np.bincount(kv, minlength=65536).astype(np.uint64)
+    wh = {"kv": kv, "mu": mu, "sigma": sigma, "counts": counts}
+    wd = {"kv": torch.from_numpy(kv.view(np.int16)).cuda().view(1, 1, 80, 1, 1024),
+          "mu": torch.from_numpy(mu.view(np.int16)).cuda().view(1, 1, 80, 1, 1024),
+          "sigma": torch.from_numpy(sigma).cuda(), "counts": torch.from_numpy(counts.view(np.int64)).cuda()}
+    H.assert_same_stream(lay, wd, wh)
+
+
+def test_all_e4m3_codes():
+    rng = np.random.default_rng(4)
+    lay = Layout("e4m3", 2, 2, 2, 64, 96, tokens_per_chunk=64)
+    n = lay.n_elems
+    kv = rng.integers(0, 256, n).astype(np.uint8)
+    kv[:256] = np.arange(256, dtype=np.uint8)
+    mu = rng.integers(0, 256, n).astype(np.uint8)
+    mu[(mu & 0x7F) == 0x7F] = 0x38
+    sigma = np.exp(rng.normal(0, 2, 2 * 2 * 128)).astype(np.float32)
+    counts = np.bincount(kv, minlength=256).astype(np.uint64)
+    shp = (2, 2, 96, 2, 64)
+    wh = {"kv": kv, "mu": mu, "sigma": sigma, "counts": counts}
+    wd = {"kv": torch.from_numpy(kv).cuda().view(shp), "mu": torch.from_numpy(mu).cuda().view(shp),
+          "sigma": torch.from_numpy(sigma).cuda(), "counts": torch.from_numpy(counts.view(np.int64)).cuda()}
+    H.assert_same_stream(lay, wd, wh)
+
+
+def test_predictor_equal_to_target():
+    cfg = synth.CONFIGS["tiny"]
+    wd, wh = _workload(cfg)
+    wd["mu"] = wd["kv"].clone()
+    wh["mu"] = wh["kv"].copy()
+    wd["sigma"] = torch.full_like(wd["sigma"], 2.0 ** -126)
+    wh["sigma"] = np.full_like(wh["sigma"], 2.0 ** -126)
+    s, offs, _ = H.assert_same_stream(H.layout_of(cfg), wd, wh)
+    assert 8.0 * s.numel() / cfg.n_elems < 0.1
+
+
+# -------------------------------------------------------------- page access
+
+def test_decode_chunks_pages():
+    cfg = synth.CONFIGS["paged_14b"].scaled(n_layers=1, n_tokens=1000, calib_tokens=512)
+    wd, wh = _workload(cfg)
+    lay = H.layout_of(cfg)
+    c = Coder(lay)
+    s, offs = c.encode(wd["kv"], wd["mu"], wd["sigma"], wd["counts"])
+    ids = torch.tensor([5, 0, 3, 7, 3], dtype=torch.int32, device="cuda")
+    pages = c.decode_chunks(s, offs, wd["mu"], wd["sigma"], wd["counts"], ids)
+    want = O.decode_pages(H.o_layout(lay), s.cpu().numpy(), offs.cpu().numpy().astype(np.uint64),
+                          wh["mu"], wh["sigma"], wh["counts"], ids.cpu().numpy().astype(np.uint64))
+    got = pages.cpu().numpy().view(np.uint16)
+    # chunk 7 is the short last page of plane 1 (1000 = 3 * 256 + 232 tokens)
+    for i, k in enumerate(ids.tolist()):
+        ntok = 232 if k in (3, 7) else 256
+        n = ntok * 1024
+        assert np.array_equal(got[i, :n], want[i, :n]), k
+        plane, page = divmod(k, 4)
+        ref = wh["kv"].reshape(2, 1000 * 1024)[plane, page * 256 * 1024: page * 256 * 1024 + n]
+        assert np.array_equal(got[i, :n], ref)
+
+
+def test_decode_chunks_rejects_bad_id():
+    cfg = synth.CONFIGS["tiny"]
+    wd, _ = _workload(cfg)
+    c = Coder(H.layout_of(cfg))
+    s, offs = c.encode(wd["kv"], wd["mu"], wd["sigma"], wd["counts"])
+    ids = torch.tensor([0, 2], dtype=torch.int32, device="cuda")
+    with pytest.raises(SKVError) as e:
+        c.decode_chunks(s, offs, wd["mu"], wd["sigma"], wd["counts"], ids)
+    assert e.value.name == "INVALID_ARG"
+
+
+# ------------------------------------------------------------------ errors
+
+def test_status_errors():
+    cfg = synth.CONFIGS["tiny"]
+    wd, _ = _workload(cfg)
+    lay = H.layout_of(cfg)
+    c = Coder(lay)
+    sig = wd["sigma"].clone()
+    sig.view(-1)[7] = float("nan")
+    with pytest.raises(SKVError) as e:
+        c.encode(wd["kv"], wd["mu"], sig, wd["counts"])
+    assert e.value.name == "BAD_SIGMA"
+    mu = wd["mu"].clone()
+    mu.view(-1)[123] = 0x7F80
+    with pytest.raises(SKVError) as e:
+        c.encode(wd["kv"], mu, wd["sigma"], wd["counts"])
+    assert e.value.name == "NONFINITE_MU"
+    with pytest.raises(SKVError) as e:
+        c.encode(wd["kv"], wd["mu"], wd["sigma"], torch.zeros_like(wd["counts"]))
+    assert e.value.name == "EMPTY_MARGINAL"
+    out, offs = c.alloc_output()
+    small = out[: 100000]
+    c.encode_into(wd["kv"], wd["mu"], wd["sigma"], wd["counts"], small, offs)
+    with pytest.raises(SKVError) as e:
+        c.check_status("encode")
+    assert e.value.name == "CAPACITY"
+    assert int(offs[-1]) > 100000
+
+
+def test_corruption_detected():
+    cfg = synth.CONFIGS["tiny"]
+    wd, _ = _workload(cfg)
+    c = Coder(H.layout_of(cfg))
+    s, offs = c.encode(wd["kv"], wd["mu"], wd["sigma"], wd["counts"])
+    rng = np.random.default_rng(1)
+    for _ in range(6):
+        bad = s.clone()
+        pos = int(rng.integers(8 * 64 + 64, int(offs[1]) - 64))
+        bad[pos] ^= 1 << int(rng.integers(0, 8))
+        with pytest.raises(SKVError) as e:
+            c.decode(bad, offs, wd["mu"], wd["sigma"], wd["counts"])
+        assert e.value.name == "CORRUPT"
+    with pytest.raises(SKVError):
+        c.decode(s[:-16], offs, wd["mu"], wd["sigma"], wd["counts"])
+    bo = offs.clone()
+    bo[1] += 16
+    with pytest.raises(SKVError):
+        c.decode(s, bo, wd["mu"], wd["sigma"], wd["counts"])
+    bad = s.clone()
+    bad[7] = 0xFF
+    with pytest.raises(SKVError):
+        c.decode(bad, offs, wd["mu"], wd["sigma"], wd["counts"])
+    # the context is still usable after all of the above
+    back = c.decode(s, offs, wd["mu"], wd["sigma"], wd["counts"])
+    assert torch.equal(back, wd["kv"])
+
+
+# -------------------------------------------------------------- full sizes
+
+FULL = ["qwen3_0p6b", "qwen3_8b", "fp8_32b", "paged_14b"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(name):
+    cfg = synth.CONFIGS[name]
+    wd = synth.generate(cfg, device="cuda")
+    lay = H.layout_of(cfg)
+    c = Coder(lay)
+    s, offs = c.encode(wd["kv"], wd["mu"], wd["sigma"], wd["counts"])
+    back = torch.empty_like(wd["mu"])
+    c.decode_into(s, offs, wd["mu"], wd["sigma"], wd["counts"], back)
+    c.check_status("decode")
+    assert torch.equal(back, wd["kv"])
+    del back
+    rng = np.random.default_rng(hash(name) % 1000)
+    n = lay.n_chunks
+    ks = sorted(set([0, n - 1] + rng.integers(0, n, 3).tolist()))
+    offs_h = offs.cpu().numpy()
+    for k in ks:
+        sub, part = H.slice_chunk(lay, wd, k)
+        so, oo = O.encode(H.o_layout(sub), part["kv"], part["mu"], part["sigma"], part["counts"])
+        got = s[int(offs_h[k]):int(offs_h[k + 1])].cpu().numpy()
+        assert np.array_equal(got, so), (name, k)
+    bits = 8.0 * float(offs_h[-1]) / lay.n_elems
+    assert bits < (7.0 if lay.dtype == "bf16" else 4.0), bits
