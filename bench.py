@@ -163,12 +163,17 @@ def main():
     ap.add_argument("--ref-chunks", type=int, default=8, help="chunks per oracle step")
     ap.add_argument("--cpu-chunks", type=int, default=16, help="chunks in the cpu_baseline sample")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
+    ap.add_argument("--layers", type=int, default=None, help="override n_layers (profiling cases)")
+    ap.add_argument("--tokens", type=int, default=None, help="override n_tokens (profiling cases)")
     ap.add_argument("--traffic-json", default=os.path.join(ROOT, "profiles", "traffic.json"))
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "skv" else args.warmup
 
     from lossless_kv_cache_scalar_gb300 import synth
     cfg = synth.CONFIGS[args.config]
+    if args.layers or args.tokens:
+        cfg = cfg.scaled(n_layers=args.layers, n_tokens=args.tokens)
     if args.impl == "reference":
         return run_reference(args, cfg)
 
@@ -254,12 +259,15 @@ def main():
     line = None
     if rank == 0:
         cpu = None
-        try:
+        if args.no_cpu:
+            cpu = {"value": None, "unit": "GB/s", "cores": None, "kind": "oracle", "sample": "skipped (--no-cpu)"}
+        else:
+          try:
             from oracle import oracle as O
             nb, dt, desc = cpu_oracle_run(cfg, args.cpu_chunks, O.threads())
             cpu = {"value": nb / dt / 1e9, "unit": "GB/s", "cores": O.threads(), "kind": "oracle",
                    "sample": desc}
-        except Exception as e:  # the baseline must not hide the GPU number
+          except Exception as e:  # the baseline must not hide the GPU number
             cpu = {"value": None, "unit": "GB/s", "cores": None, "kind": "oracle", "sample": f"failed: {e}"}
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
