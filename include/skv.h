@@ -189,6 +189,35 @@ int32_t skv_cdf_eval(const skv_layout *lay, const uint64_t *counts, uint64_t n,
                      uint32_t *C_out, int32_t *status, void *workspace, uint64_t ws_bytes,
                      void *stream);
 
+/*
+ * Decode without any caller-provided scratch (the pages describe no such
+ * call; it serves deployment only). Same contract and outputs as skv_decode,
+ * minus the workspace arguments. It is meant for callers that cannot call
+ * cudaMalloc or lend a workspace: a host program whose memory pool owns all
+ * device memory and gives this library no allocator, or a latency-critical
+ * path where allocating (and the device-wide synchronisation that freeing
+ * brings) is not allowed.
+ *
+ * Its scratch is a fixed device array of SKV_NOALLOC_SCRATCH_BYTES inside the
+ * library, held by every GPU that loads the library until the process exits.
+ * Layouts whose decode scratch (skv_workspace_bytes(lay, 0, ...): the P_hat
+ * table plus 4 bytes per (layer, kv, channel)) exceeds it are rejected with
+ * SKV_ERR_INVALID_ARG before anything is enqueued; 1 MiB covers a bf16 cache
+ * of up to 196,544 (layer, kv, channel) sigmas, e.g. 80 planes (40 layers, K and V)
+ * of 2,048 channels.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture. Every call
+ * on a device shares the one array and each call rewrites all of it that it
+ * reads, so nothing carries over between calls; calls that overlap on the GPU
+ * (on different streams, or from several host threads) race on it and must be
+ * serialised by the caller. No memory is allocated or freed.
+ */
+#define SKV_NOALLOC_SCRATCH_BYTES (1u << 20)
+int32_t skv_decode_noalloc(const skv_layout *lay, const void *bitstream, uint64_t bitstream_bytes,
+                           const uint64_t *offsets, const void *mu, const float *sigma,
+                           const uint64_t *counts, void *kv_out, int32_t *status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -42,6 +42,7 @@ SIGNATURES = {
     "skv_decode_chunks": (_i32, [_LP, _vp, _u64, _vp, _vp, _vp, _vp, _vp, _u32, _vp, _vp, _vp,
                                  _u64, _vp]),
     "skv_cdf_eval": (_i32, [_LP, _vp, _u64, _vp, _vp, _vp, _vp, _vp, _vp, _u64, _vp]),
+    "skv_decode_noalloc": (_i32, [_LP, _vp, _u64, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
 }
 
 _lib = None
