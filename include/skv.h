@@ -117,13 +117,19 @@ int32_t skv_num_chunks(const skv_layout *lay, uint64_t *n_chunks);
 int32_t skv_max_encoded_bytes(const skv_layout *lay, uint64_t *bytes);
 
 /*
- * Device workspace bytes needed by skv_encode (encode != 0) or by
- * skv_decode / skv_decode_chunks (encode == 0). The workspace must be
- * 256-byte aligned and must not be used by another call in flight.
- * Encode holds one worst-case word slot per stream group (about the size of
- * skv_max_encoded_bytes); decode holds only the tables (< 1 MB).
+ * Device workspace bytes for a call on this layout, by op:
+ *   1  skv_encode: the tables plus one worst-case word slot per stream group
+ *      (about the size of skv_max_encoded_bytes);
+ *   0  skv_decode / skv_decode_chunks, minimum: the P_hat, 1/sigma and
+ *      quantile tables (< 1 MB for these shapes);
+ *   2  skv_decode / skv_decode_chunks with the outlier inverse tables as well
+ *      (+ 4 * 2^m bytes: 64 MiB for bf16, 256 KiB for e4m3), which make far
+ *      outliers cost one lookup instead of a bisection. A decode call uses
+ *      these tables whenever ws_bytes is at least this size; the decoded
+ *      output is the same either way.
+ * The workspace must be 256-byte aligned and not used by another call in flight.
  */
-int32_t skv_workspace_bytes(const skv_layout *lay, int32_t encode, uint64_t *bytes);
+int32_t skv_workspace_bytes(const skv_layout *lay, int32_t op, uint64_t *bytes);
 
 /*
  * Encode a whole KV cache (the encoder of the wiki's pipeline section).
@@ -150,7 +156,7 @@ int32_t skv_encode(const skv_layout *lay, const void *kv, const void *mu, const 
  *  offsets       device uint64[n_chunks + 1] as written by skv_encode
  *  mu, sigma, counts   exactly as given to skv_encode
  *  kv_out        device, codes in canonical layout, 16-byte aligned
- *  workspace     device, ws_bytes >= skv_workspace_bytes(lay, 0)
+ *  workspace     device, ws_bytes >= skv_workspace_bytes(lay, 0) (or op 2, faster)
  * Device errors: CORRUPT (the chunk's output is then unspecified),
  * NONFINITE_MU, BAD_SIGMA, EMPTY_MARGINAL.
  */
@@ -200,11 +206,12 @@ int32_t skv_cdf_eval(const skv_layout *lay, const uint64_t *counts, uint64_t n,
  *
  * Its scratch is a fixed device array of SKV_NOALLOC_SCRATCH_BYTES inside the
  * library, held by every GPU that loads the library until the process exits.
- * Layouts whose decode scratch (skv_workspace_bytes(lay, 0, ...): the P_hat
- * table plus 4 bytes per (layer, kv, channel)) exceeds it are rejected with
- * SKV_ERR_INVALID_ARG before anything is enqueued; 1 MiB covers a bf16 cache
- * of up to 196,544 (layer, kv, channel) sigmas, e.g. 80 planes (40 layers, K and V)
- * of 2,048 channels.
+ * Layouts whose minimum decode scratch (skv_workspace_bytes(lay, 0, ...): the
+ * P_hat and quantile tables plus 4 bytes per (layer, kv, channel)) exceeds it
+ * are rejected with SKV_ERR_INVALID_ARG before anything is enqueued; 1 MiB
+ * covers a bf16 cache of up to 191,360 (layer, kv, channel) sigmas, e.g. 80
+ * planes (40 layers, K and V) of 2,048 channels. The outlier inverse tables do
+ * not fit, so far outliers are found by bisection (same output, slower).
  *
  * The first call on a device looks up the array's device address (with that
  * device current); make that first call before any stream capture. Every call

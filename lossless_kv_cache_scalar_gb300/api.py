@@ -64,8 +64,11 @@ class Layout:
     def max_encoded_bytes(self) -> int:
         return self._q(B.lib().skv_max_encoded_bytes)
 
-    def workspace_bytes(self, encode: bool) -> int:
-        return self._q(B.lib().skv_workspace_bytes, 1 if encode else 0)
+    def workspace_bytes(self, encode: bool, fast: bool = True) -> int:
+        """Workspace of skv_encode (encode=True) or of the decoders; fast=True
+        includes the outlier inverse tables (op 2), fast=False is the minimum."""
+        op = 1 if encode else (2 if fast else 0)
+        return self._q(B.lib().skv_workspace_bytes, op)
 
     @classmethod
     def for_tensor(cls, kv: torch.Tensor, dtype: str | None = None, **kw) -> "Layout":
@@ -99,7 +102,7 @@ class Coder:
     """
 
     def __init__(self, layout: Layout, device: torch.device | str | int = "cuda",
-                 encode: bool = True, decode: bool = True):
+                 encode: bool = True, decode: bool = True, fast_decode: bool = True):
         self.layout = layout
         self.device = torch.device(device)
         self._c = layout.c()
@@ -107,7 +110,7 @@ class Coder:
         if encode:
             need = max(need, layout.workspace_bytes(True))
         if decode:
-            need = max(need, layout.workspace_bytes(False))
+            need = max(need, layout.workspace_bytes(False, fast_decode))
         self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.n_chunks = layout.n_chunks

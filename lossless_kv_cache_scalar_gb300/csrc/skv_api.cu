@@ -13,6 +13,8 @@ int launch_encode(const EncArgs &a, cudaStream_t st);
 int launch_scan(const ScanArgs &a, cudaStream_t st);
 int launch_compact(const CompactArgs &a, cudaStream_t st);
 int launch_decode(const DecArgs &a, cudaStream_t st);
+int launch_search_aids(const Geom &g, const uint32_t *phat, float *qt, uint16_t *inv_lo,
+                       uint16_t *inv_hi, cudaStream_t st);
 
 // ------------------------------------------------------------- set-up kernel
 
@@ -171,6 +173,8 @@ static uint64_t chunk_max_bytes(const Geom &g, uint64_t n_vec) {
 struct Workspace {
     uint32_t *phat;
     float *rsig;
+    float *qt;
+    uint16_t *inv_lo, *inv_hi;
     uint64_t *states;
     uint32_t *nwords;
     uint32_t *scratch;
@@ -179,31 +183,51 @@ struct Workspace {
 
 static uint64_t round256(uint64_t b) { return (b + 255u) & ~uint64_t(255); }
 
-static Workspace carve(const Geom &g, bool encode, uint8_t *base) {
+// Workspace kinds: the encoder's, the decoder's minimum, and the decoder's
+// with the outlier inverse tables (faster on data with far outliers).
+enum WsKind { WS_ENCODE = 1, WS_DECODE_MIN = 0, WS_DECODE_FULL = 2 };
+
+static Workspace carve(const Geom &g, int kind, uint8_t *base) {
     // offsets are computed as integers and only then turned into pointers
     const DtypeInfo d = dtype_info(g.dtype);
-    uint64_t off = 0, o_phat, o_rsig, o_states = 0, o_nwords = 0, o_scratch = 0;
+    uint64_t off = 0, o_phat, o_rsig, o_qt = 0, o_lo = 0, o_hi = 0, o_states = 0, o_nwords = 0,
+             o_scratch = 0;
     o_phat = off;
     off += round256(4ull * (d.N + 1));
     o_rsig = off;
     off += round256(4ull * g.n_planes * g.HD);
-    if (encode) {
+    if (kind == WS_ENCODE) {
         o_states = off;
         off += round256(8ull * 32ull * g.n_groups);
         o_nwords = off;
         off += round256(4ull * g.n_groups);
         o_scratch = off;
         off += round256(4ull * g.cap_words * g.n_groups);
+    } else {
+        o_qt = off;
+        off += round256(4ull * kQuantFloats);
+        if (kind == WS_DECODE_FULL) {
+            o_lo = off;
+            off += round256(2ull << d.m);
+            o_hi = off;
+            off += round256(2ull << d.m);
+        }
     }
     Workspace w{};
     w.bytes = off;
     if (base) {
         w.phat = reinterpret_cast<uint32_t *>(base + o_phat);
         w.rsig = reinterpret_cast<float *>(base + o_rsig);
-        if (encode) {
+        if (kind == WS_ENCODE) {
             w.states = reinterpret_cast<uint64_t *>(base + o_states);
             w.nwords = reinterpret_cast<uint32_t *>(base + o_nwords);
             w.scratch = reinterpret_cast<uint32_t *>(base + o_scratch);
+        } else {
+            w.qt = reinterpret_cast<float *>(base + o_qt);
+            if (kind == WS_DECODE_FULL) {
+                w.inv_lo = reinterpret_cast<uint16_t *>(base + o_lo);
+                w.inv_hi = reinterpret_cast<uint16_t *>(base + o_hi);
+            }
         }
     }
     return w;
@@ -218,11 +242,11 @@ static int32_t run_setup(const Geom &g, const float *sigma, const uint64_t *coun
 }
 
 static int32_t common_checks(const Geom &g, const float *sigma, const uint64_t *counts,
-                             int32_t *status, void *workspace, uint64_t ws_bytes, bool encode) {
+                             int32_t *status, void *workspace, uint64_t ws_bytes, int kind) {
     if (!sigma || !status || !workspace) return SKV_ERR_INVALID_ARG;
     if (g.w_h && !counts) return SKV_ERR_INVALID_ARG;
     if (((uintptr_t)workspace & 255u) != 0) return SKV_ERR_INVALID_ARG;
-    if (ws_bytes < carve(g, encode, nullptr).bytes) return SKV_ERR_INVALID_ARG;
+    if (ws_bytes < carve(g, kind, nullptr).bytes) return SKV_ERR_INVALID_ARG;
     return SKV_OK;
 }
 
@@ -293,10 +317,11 @@ int32_t skv_max_encoded_bytes(const skv_layout *lay, uint64_t *bytes) {
     return SKV_OK;
 }
 
-int32_t skv_workspace_bytes(const skv_layout *lay, int32_t encode, uint64_t *bytes) {
+int32_t skv_workspace_bytes(const skv_layout *lay, int32_t op, uint64_t *bytes) {
     Geom g;
     if (make_geom(lay, g) != SKV_OK || !bytes) return SKV_ERR_INVALID_ARG;
-    *bytes = carve(g, encode != 0, nullptr).bytes;
+    if (op != WS_ENCODE && op != WS_DECODE_MIN && op != WS_DECODE_FULL) return SKV_ERR_INVALID_ARG;
+    *bytes = carve(g, op, nullptr).bytes;
     return SKV_OK;
 }
 
@@ -306,13 +331,13 @@ int32_t skv_encode(const skv_layout *lay, const void *kv, const void *mu, const 
     Geom g;
     int32_t r = make_geom(lay, g);
     if (r != SKV_OK) return r;
-    r = common_checks(g, sigma, counts, status, workspace, ws_bytes, true);
+    r = common_checks(g, sigma, counts, status, workspace, ws_bytes, WS_ENCODE);
     if (r != SKV_OK) return r;
     if (!offsets || (g.n_chunks && (!kv || !mu || !out))) return SKV_ERR_INVALID_ARG;
     if (g.n_chunks && (!aligned16(kv) || !aligned16(mu) || !aligned16(out))) return SKV_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return SKV_ERR_CUDA;
-    const Workspace ws = carve(g, true, static_cast<uint8_t *>(workspace));
+    const Workspace ws = carve(g, WS_ENCODE, static_cast<uint8_t *>(workspace));
     if ((r = run_setup(g, sigma, counts, ws, status, st)) != SKV_OK) return r;
     EncArgs ea{g, static_cast<const uint8_t *>(kv), static_cast<const uint8_t *>(mu), ws.phat,
                ws.rsig, ws.states, ws.nwords, ws.scratch, status};
@@ -333,7 +358,7 @@ static int32_t decode_impl(const skv_layout *lay, const void *bitstream, uint64_
     Geom g;
     int32_t r = make_geom(lay, g);
     if (r != SKV_OK) return r;
-    r = common_checks(g, sigma, counts, status, workspace, ws_bytes, false);
+    r = common_checks(g, sigma, counts, status, workspace, ws_bytes, WS_DECODE_MIN);
     if (r != SKV_OK) return r;
     if (!pages) n_units = g.n_chunks;
     if (n_units && (!bitstream || !offsets || !mu || !out)) return SKV_ERR_INVALID_ARG;
@@ -341,10 +366,14 @@ static int32_t decode_impl(const skv_layout *lay, const void *bitstream, uint64_
     if (n_units && (!aligned16(bitstream) || !aligned16(mu) || !aligned16(out))) return SKV_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return SKV_ERR_CUDA;
-    const Workspace ws = carve(g, false, static_cast<uint8_t *>(workspace));
+    const int kind = ws_bytes >= carve(g, WS_DECODE_FULL, nullptr).bytes ? WS_DECODE_FULL : WS_DECODE_MIN;
+    const Workspace ws = carve(g, kind, static_cast<uint8_t *>(workspace));
     if ((r = run_setup(g, sigma, counts, ws, status, st)) != SKV_OK) return r;
+    if (n_units == 0) return SKV_OK;
+    if (launch_search_aids(g, ws.phat, ws.qt, ws.inv_lo, ws.inv_hi, st)) return SKV_ERR_CUDA;
     DecArgs da{g, static_cast<const uint8_t *>(bitstream), bitstream_bytes, offsets,
-               static_cast<const uint8_t *>(mu), ws.phat, ws.rsig, pages ? ids : nullptr,
+               static_cast<const uint8_t *>(mu), ws.phat, ws.rsig, ws.qt, ws.inv_lo, ws.inv_hi,
+               pages ? ids : nullptr,
                n_units, static_cast<uint8_t *>(out), (uint64_t)g.Tc * g.HD, status};
     if (launch_decode(da, st)) return SKV_ERR_CUDA;
     return SKV_OK;
@@ -376,11 +405,11 @@ int32_t skv_cdf_eval(const skv_layout *lay, const uint64_t *counts, uint64_t n,
     if (r != SKV_OK) return r;
     if (!status || !workspace || (g.w_h && !counts)) return SKV_ERR_INVALID_ARG;
     if (n && (!mu_codes || !sigmas || !ords || !C_out)) return SKV_ERR_INVALID_ARG;
-    if (((uintptr_t)workspace & 255u) != 0 || ws_bytes < carve(g, false, nullptr).bytes)
+    if (((uintptr_t)workspace & 255u) != 0 || ws_bytes < carve(g, WS_DECODE_MIN, nullptr).bytes)
         return SKV_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return SKV_ERR_CUDA;
-    const Workspace ws = carve(g, false, static_cast<uint8_t *>(workspace));
+    const Workspace ws = carve(g, WS_DECODE_MIN, static_cast<uint8_t *>(workspace));
     // P_hat only; sigma is per query here, so rsig is not built
     Geom g1 = g;
     g1.n_planes = 0;

@@ -1,15 +1,29 @@
-// skv_decode.cu -- decoder kernel: CDF inversion fused with the rANS state
-// update and word refill (FORMAT.md sections 5-7).
+// skv_decode.cu -- decoder: CDF inversion fused with the rANS state update and
+// word refill (FORMAT.md sections 5-7), plus the per-call search aids.
 //
 // The decoder of the Speculative KV Coding wiki's pipeline section: from the
 // bits and the same (mu, sigma) it restores every code exactly. One warp
 // decodes one group of 32 streams; lane l is stream 32 g + l and walks its
 // vectors in increasing order. Per scalar: slot = x mod M, find the code o
-// with C(o) <= slot < C(o+1) by a search over the monotone code order that
-// starts at mu's own code, update x, and refill one 32-bit word when x falls
-// below L. Words are consumed in ascending lane order per step (a ballot gives
-// each lane its index); they are staged in a per-warp shared-memory ring by
-// cp.async so the refill never waits on global memory.
+// with C(o) <= slot < C(o+1), update x, and refill one 32-bit word when x
+// falls below L. Words are consumed in ascending lane order per step (a
+// ballot gives each lane its index) from a per-warp shared-memory ring that
+// cp.async keeps ahead of the reader.
+//
+// Finding o. The exact test is two evaluations of C, the same two the
+// encoder makes. Where to test is estimated by inverting the Gaussian part of
+// the mixture: with p_hat's share and the floor term taken at a reference
+// code, the slot gives a quantile g of G(z) = (w_n Phi(z) + w_w Phi(z/3)) /
+// (w_n + w_w); a table in t = -log2(min(g, 1 - g)) gives z = G^-1(g); and
+// mu + z sigma rounded to the code grid is the estimate (a code owns the reals
+// that round to it, FORMAT.md section 2). A first pass takes the reference at
+// mu's own code, a second at the first estimate. A far outlier that only
+// p_hat explains (both Gaussians saturated, so C is a mu-independent function
+// of o) is read from per-call inverse tables instead. When the test fails,
+// Newton steps in code space (using each probe's own code width) inside a
+// shrinking bracket, then bisection, find the code. Search aids change speed
+// only; the decoded codes are fixed by the exact test.
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "skv_model.cuh"
@@ -17,48 +31,232 @@
 namespace skv {
 
 constexpr int kDecWarps = 8;
-constexpr uint32_t kRing = 1024;       // words per warp ring
-constexpr uint32_t kBlock = 256;       // words per cp.async batch (2 x 16 B per lane)
+constexpr uint32_t kRing = 512;        // words per warp ring
+constexpr uint32_t kBlock = 128;       // words per cp.async batch (16 B per lane)
+constexpr uint32_t kStepSyms = 8;      // the ring is topped up every 8 symbols
 
-// The code o with C(o) <= s < C(o+1), and its (c, f). C(0) = 0 <= s and
-// C(N) = M > s hold by construction, so the ends are never evaluated. The
-// search gallops away from o0 (mu's own code) and then bisects.
-template <uint32_t DT>
-__device__ __forceinline__ uint32_t find_symbol(const Tables &t, const Tables8 *t8, const Weights w,
-                                                const uint32_t *__restrict__ phat, uint32_t s,
-                                                float mu, float rs, uint32_t o0, uint32_t &c_out,
-                                                uint32_t &f_out) {
-    using K = Codes<DT>;
-    constexpr uint32_t M = 1u << K::m;
-    uint32_t lo, hi, clo, chi;
-    const uint32_t c0 = cdf<DT>(t, t8, w, phat, o0, mu, rs);
-    uint32_t step = 1;
-    if (s >= c0) {
-        lo = o0; clo = c0;
-        for (;;) {
-            hi = min(lo + step, K::N);
-            chi = (hi == K::N) ? M : cdf<DT>(t, t8, w, phat, hi, mu, rs);
-            if (chi > s) break;
-            lo = hi; clo = chi; step <<= 1;
-        }
-    } else {
-        hi = o0; chi = c0;
-        for (;;) {
-            lo = hi > step ? hi - step : 0u;
-            clo = (lo == 0u) ? 0u : cdf<DT>(t, t8, w, phat, lo, mu, rs);
-            if (clo <= s) break;
-            hi = lo; chi = clo; step <<= 1;
-        }
+// dynamic shared memory layout (bytes)
+constexpr uint32_t kSmPhi = 0;                                        // Tables
+constexpr uint32_t kSmQt = (sizeof(Tables) + 15u) & ~15u;              // float2[kQuantN + 1]
+constexpr uint32_t kSmT8 = (kSmQt + 8u * (kQuantN + 1) + 15u) & ~15u;  // Tables8
+constexpr uint32_t kSmRing = (kSmT8 + sizeof(Tables8) + 15u) & ~15u;   // uint32 [warps][kRing]
+constexpr uint32_t kDecSmem = kSmRing + kDecWarps * kRing * 4u;
+
+// ------------------------------------------------------------ search aids
+
+// G(z) = (w_n Phi(z) + w_w Phi(z/3)) / (w_n + w_w), the Gaussian part of the mixture.
+__device__ float gauss_part(float z, float wn, float ww) {
+    return (wn * normcdff(z) + ww * normcdff(z / 3.0f)) / (wn + ww);
+}
+
+__device__ float gauss_quantile(float g, float wn, float ww) {
+    float lo = -64.0f, hi = 64.0f;
+    for (int it = 0; it < 60; ++it) {
+        const float mid = 0.5f * (lo + hi);
+        if (gauss_part(mid, wn, ww) < g) lo = mid; else hi = mid;
     }
+    return 0.5f * (lo + hi);
+}
+
+// qt[i] = (z_i, z_{i+1} - z_i), z_i = G^-1(2^-(1 + i/64)), i = 0..kQuantN.
+__global__ void __launch_bounds__(256) quant_kernel(const QuantArgs a) {
+    const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i > kQuantN) return;
+    float z0 = 0.0f, z1 = 0.0f;
+    if (a.w_n + a.w_w != 0u) {
+        const float wn = (float)a.w_n, ww = (float)a.w_w;
+        z0 = gauss_quantile(exp2f(-(1.0f + (float)i / kQuantSteps)), wn, ww);
+        z1 = (i < kQuantN) ? gauss_quantile(exp2f(-(1.0f + (float)(i + 1) / kQuantSteps)), wn, ww) : z0;
+    }
+    a.qt[2 * i] = z0;
+    a.qt[2 * i + 1] = z1 - z0;
+}
+
+// C with both Gaussians saturated: base = 0 below mu (z <= -24), or
+// (w_n + w_w) 2^24 above (z >= 24); then C depends on o alone.
+template <uint32_t DT>
+__device__ __forceinline__ uint32_t c_saturated(uint32_t o, uint32_t base, uint32_t wh,
+                                                const uint32_t *__restrict__ phat) {
+    constexpr uint32_t MN = (1u << Codes<DT>::m) - Codes<DT>::N;
+    const uint32_t S = base + wh * __ldg(phat + o);
+    return o + (uint32_t)(((uint64_t)S * MN) >> 24) / 100u;
+}
+
+// max{o in [lo, hi) : C_sat(o) <= s}, or lo when there is none; C_sat(o) is
+// c_saturated with the given base, non-decreasing in o.
+template <uint32_t DT>
+__device__ uint32_t sat_search(uint32_t s, uint32_t base, uint32_t wh, const uint32_t *__restrict__ phat,
+                               uint32_t lo, uint32_t hi) {
     while (hi - lo > 1u) {
         const uint32_t mid = (lo + hi) >> 1;
-        const uint32_t cm = cdf<DT>(t, t8, w, phat, mid, mu, rs);
-        if (cm <= s) { lo = mid; clo = cm; } else { hi = mid; chi = cm; }
+        if (c_saturated<DT>(mid, base, wh, phat) <= s) lo = mid; else hi = mid;
     }
-    c_out = clo;
-    f_out = chi - clo;
     return lo;
 }
+
+// inv_lo[s] = max{o < N : C_lo(o) <= s}; inv_hi[s] = max{o < N : C_hi(o) <= s}, 0 if none.
+// One block per 256 slots (blockIdx.y picks the table): two searches over all
+// codes bound the block's answers, then each slot searches that short range.
+template <uint32_t DT>
+__global__ void __launch_bounds__(256) inv_kernel(const InvArgs a) {
+    using K = Codes<DT>;
+    const uint32_t base = blockIdx.y ? (a.g.w_n + a.g.w_w) << 24 : 0u;
+    uint16_t *out = blockIdx.y ? a.inv_hi : a.inv_lo;
+    __shared__ uint32_t range[2];
+    const uint32_t s0 = blockIdx.x * 256u;
+    if (threadIdx.x < 2)
+        range[threadIdx.x] = sat_search<DT>(s0 + 255u * threadIdx.x, base, a.g.w_h, a.phat, 0u, K::N);
+    __syncthreads();
+    const uint32_t s = s0 + threadIdx.x;
+    out[s] = (uint16_t)sat_search<DT>(s, base, a.g.w_h, a.phat, range[0], range[1] + 1u);
+}
+
+int launch_search_aids(const Geom &g, const uint32_t *phat, float *qt, uint16_t *inv_lo,
+                       uint16_t *inv_hi, cudaStream_t st) {
+    QuantArgs qa{g.w_n, g.w_w, qt};
+    quant_kernel<<<(kQuantN + 1 + 255) / 256, 256, 0, st>>>(qa);
+    if (cudaGetLastError() != cudaSuccess) return 1;
+    if (inv_lo) {
+        InvArgs ia{g, phat, inv_lo, inv_hi};
+        if (g.dtype == SKV_BF16) inv_kernel<SKV_BF16><<<dim3((1u << 24) / 256, 2), 256, 0, st>>>(ia);
+        else inv_kernel<SKV_E4M3><<<dim3((1u << 16) / 256, 2), 256, 0, st>>>(ia);
+        if (cudaGetLastError() != cudaSuccess) return 1;
+    }
+    return 0;
+}
+
+// ------------------------------------------------------------- the search
+
+extern __shared__ __align__(16) uint8_t skv_dec_smem[];
+
+__device__ __forceinline__ const Tables &dtab() {
+    return *reinterpret_cast<const Tables *>(skv_dec_smem + kSmPhi);
+}
+__device__ __forceinline__ const Tables8 *dtab8() {
+    return reinterpret_cast<const Tables8 *>(skv_dec_smem + kSmT8);
+}
+__device__ __forceinline__ const float2 *dqt() {
+    return reinterpret_cast<const float2 *>(skv_dec_smem + kSmQt);
+}
+
+// Round a value to the nearest code (ties to even), clamped to the finite codes.
+template <uint32_t DT> __device__ __forceinline__ uint32_t nearest_ord(float x);
+template <> __device__ __forceinline__ uint32_t nearest_ord<SKV_BF16>(float x) {
+    const uint32_t b = __float_as_uint(x);
+    const uint32_t code = (b + 0x7FFFu + ((b >> 16) & 1u)) >> 16;
+    const uint32_t o = Codes<SKV_BF16>::ord(code & 0xFFFFu);
+    return min(max(o, 0x0080u), 0xFF7Fu);
+}
+template <> __device__ __forceinline__ uint32_t nearest_ord<SKV_E4M3>(float x) {
+    const uint32_t code = (uint32_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+    const uint32_t o = Codes<SKV_E4M3>::ord(code & 0xFFu);
+    return min(max(o, 0x01u), 0xFEu);
+}
+
+// One estimate of the code of slot s, with p_hat's share and the floor term
+// taken at o_ref (ph_ref = P_hat(o_ref)). far: the quantile is within 2^-40 of
+// an end, where only p_hat and the floor hold mass; below: nearer the low end.
+template <uint32_t DT>
+__device__ __forceinline__ uint32_t estimate(const DecArgs &a, float kS, float inv_total,
+                                             uint32_t s, uint32_t o_ref, uint32_t ph_ref,
+                                             float mu, float sigma, bool &far, bool &below) {
+    using K = Codes<DT>;
+    constexpr int MN = (int)((1u << K::m) - K::N);
+    const float ph = (float)(a.g.w_h * ph_ref);
+    const float ph_top = (float)(a.g.w_h << 24) - ph;
+    const int d = (int)s - (int)o_ref;
+    const float g_lo = fmaxf(fmaf((float)max(d, 0), kS, -ph) * inv_total, 0.0f);
+    const float g_hi = fmaxf(fmaf((float)max(MN - d, 0), kS, -ph_top) * inv_total, 0.0f);
+    below = g_lo <= g_hi;
+    const float gt = fminf(g_lo, g_hi);
+    far = gt < 9.094947e-13f;                       // 2^-40
+    const float u = fminf(fmaxf(fmaf(-__log2f(gt), (float)kQuantSteps, -(float)kQuantSteps), 0.0f),
+                          (float)kQuantN - 0.001f);
+    const int k = (int)u;
+    const float2 e = dqt()[k];
+    const float zt = fmaf(u - (float)k, e.y, e.x);
+    return nearest_ord<DT>(fmaf(below ? zt : -zt, sigma, mu));
+}
+
+// The slow path: the estimate o failed (C(o) = clo, C(o+1) = chi). Newton
+// steps in code space, o += (s - C(o)) / f(o), using each probe's own width,
+// inside a bracket [lo, hi) with C(lo) <= s < C(hi) that every probe narrows;
+// then bisection of whatever bracket is left. Near zero, where bf16 codes are
+// dense and each owns about one slot, and in the tails, a step lands within a
+// few codes where the estimate in z could be thousands of codes off.
+template <uint32_t DT>
+__device__ __noinline__ uint32_t find_fallback(const DecArgs &a, uint32_t s, float mu, float rs,
+                                               uint32_t o, uint32_t clo, uint32_t chi,
+                                               uint32_t &c_out, uint32_t &f_out) {
+    using K = Codes<DT>;
+    constexpr uint32_t M = 1u << K::m;
+    const Tables &t = dtab();
+    const Tables8 *t8 = dtab8();
+    const Weights w{a.g.w_n, a.g.w_w, a.g.w_h};
+    // bracket: C(lo) <= s < C(hi); Clo/Chi are C there when known
+    uint32_t lo = 0, hi = K::N, Clo = 0, Chi = M;
+    if (s < clo) { hi = o; Chi = clo; } else { lo = o + 1u; Clo = chi; }
+    uint32_t oc = o, cc = clo, fc = chi - clo;
+    for (int it = 0; it < 6 && hi - lo > 1u; ++it) {
+        // Newton step from (oc, C(oc), f(oc)), kept strictly inside the bracket
+        const float step = ((float)s - (float)cc) / (float)fc;
+        const float fo = fminf(fmaxf((float)oc + floorf(step), (float)lo), (float)(hi - 1u));
+        const uint32_t cand = (uint32_t)fo;
+        const uint32_t ca = (cand == lo && lo == o + 1u) ? chi : cdf<DT>(t, t8, w, a.phat, cand, mu, rs);
+        const uint32_t cb = (cand + 1u == hi) ? Chi : cdf<DT>(t, t8, w, a.phat, cand + 1u, mu, rs);
+        if (ca <= s && s < cb) { c_out = ca; f_out = cb - ca; return cand; }
+        if (s < ca) { hi = cand; Chi = ca; } else { lo = cand + 1u; Clo = cb; }
+        oc = cand; cc = ca; fc = cb - ca;
+    }
+    // bisection on what is left
+    while (hi - lo > 1u) {
+        const uint32_t mid = (lo + hi) >> 1;
+        const uint32_t cm = cdf<DT>(t, t8, w, a.phat, mid, mu, rs);
+        if (cm <= s) { lo = mid; Clo = cm; } else { hi = mid; Chi = cm; }
+    }
+    c_out = Clo;
+    f_out = Chi - Clo;
+    return lo;
+}
+
+// max{o < N : C_sat(o) <= s} from the per-call table, or by bisection without it.
+template <uint32_t DT>
+__device__ __forceinline__ uint32_t saturated_inverse(const DecArgs &a, uint32_t s, uint32_t base) {
+    const uint16_t *tab = base ? a.inv_hi : a.inv_lo;
+    return tab ? (uint32_t)__ldg(tab + s) : sat_search<DT>(s, base, a.g.w_h, a.phat, 0u, Codes<DT>::N);
+}
+
+// The code o with C(o) <= s < C(o+1), and (c, f) = (C(o), C(o+1) - C(o)).
+template <uint32_t DT>
+__device__ __forceinline__ uint32_t find_symbol(const DecArgs &a, float kS, float inv_total,
+                                                uint32_t s, float mu, float rs, uint32_t o_mu,
+                                                uint32_t ph_mu, uint32_t &c_out, uint32_t &f_out) {
+    using K = Codes<DT>;
+    const Weights w{a.g.w_n, a.g.w_w, a.g.w_h};
+    uint32_t o = o_mu;
+    bool far = true, below = true;
+    if (w.n + w.w) {
+        const float sigma = __fdividef(1.0f, rs);
+        o = estimate<DT>(a, kS, inv_total, s, o_mu, ph_mu, mu, sigma, far, below);
+        if (!far) {
+            // second pass: p_hat's share and the floor term at the first estimate
+            const uint32_t ph1 = w.h ? K::phat(dtab8(), a.phat, o) : 0u;
+            o = estimate<DT>(a, kS, inv_total, s, o, ph1, mu, sigma, far, below);
+        }
+    }
+    // only p_hat holds mass this far out: the saturated inverse gives the code
+    if (far) o = saturated_inverse<DT>(a, s, (below || !(w.n + w.w)) ? 0u : (w.n + w.w) << 24);
+    const uint32_t clo = cdf<DT>(dtab(), dtab8(), w, a.phat, o, mu, rs);
+    const uint32_t chi = cdf<DT>(dtab(), dtab8(), w, a.phat, o + 1u, mu, rs);
+    if (clo <= s && s < chi) {
+        c_out = clo;
+        f_out = chi - clo;
+        return o;
+    }
+    return find_fallback<DT>(a, s, mu, rs, o, clo, chi, c_out, f_out);
+}
+
+// ----------------------------------------------------------------- kernel
 
 __device__ __forceinline__ void cp_async16(uint32_t *smem, const uint32_t *gmem) {
     const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
@@ -69,21 +267,25 @@ __device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_g
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 template <uint32_t DT>
-__global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(const DecArgs a) {
+__global__ void __launch_bounds__(kDecWarps * 32, 3) decode_kernel(const DecArgs a) {
     using K = Codes<DT>;
     constexpr uint32_t V = K::V, m = K::m;
     constexpr uint32_t M = 1u << m;
     constexpr uint64_t L = K::L;
-    __shared__ Tables tab;
-    __shared__ Tables8 tab8;
-    extern __shared__ __align__(16) uint32_t ring_all[];
-    stage_tables<DT>(tab, tab8, a.phat);
+    constexpr uint32_t BITS = 8u * K::bytes;
+    constexpr uint32_t MASK = (1u << BITS) - 1u;
+    {
+        float *qt = reinterpret_cast<float *>(skv_dec_smem + kSmQt);
+        for (uint32_t i = threadIdx.x; i < kQuantFloats; i += blockDim.x) qt[i] = a.qt[i];
+        stage_tables<DT>(*reinterpret_cast<Tables *>(skv_dec_smem + kSmPhi),
+                         *reinterpret_cast<Tables8 *>(skv_dec_smem + kSmT8), a.phat);
+    }
 
     const Geom &g = a.g;
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
     const uint64_t gid = (uint64_t)blockIdx.x * kDecWarps + warp;
     if (gid >= a.n_units * g.G) return;
-    uint32_t *ring = ring_all + warp * kRing;
+    uint32_t *ring = reinterpret_cast<uint32_t *>(skv_dec_smem + kSmRing) + warp * kRing;
     const uint64_t unit = gid / g.G;
     const uint32_t grp = (uint32_t)(gid % g.G);
     const uint64_t k = a.ids ? (uint64_t)a.ids[unit] : unit;
@@ -132,7 +334,8 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(const DecArgs
     const uint8_t *mup = a.mu + cs.elem0 * K::bytes;
     const float *rsp = a.rsig + cs.plane * g.HD;
     uint8_t *outp = a.ids ? a.out + unit * a.page_elems * K::bytes : a.out + cs.elem0 * K::bytes;
-    const Weights w{g.w_n, g.w_w, g.w_h};
+    const float kS = (float)(100.0 * 16777216.0 / (double)((1u << m) - K::N));
+    const float inv_total = (g.w_n + g.w_w) ? 1.0f / ((float)(g.w_n + g.w_w) * 16777216.0f) : 0.0f;
     const uint32_t lt = lanemask_lt();
     bool bad_mu = false;
 
@@ -140,60 +343,67 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(const DecArgs
     uint32_t filled = 0;    // words requested into the ring so far (warp-uniform)
 
     uint4 mu_n = make_uint4(0, 0, 0, 0);
-    float4 rs_n[V / 4];
-    auto fetch = [&](int64_t j) {
-        if (j < nq) {
-            const uint64_t q = s + (uint64_t)j * g.W;
-            mu_n = __ldg(reinterpret_cast<const uint4 *>(mup) + q);
-            const uint32_t c0 = (uint32_t)((q * V) % g.HD);
-#pragma unroll
-            for (int i = 0; i < (int)(V / 4); ++i)
-                rs_n[i] = __ldg(reinterpret_cast<const float4 *>(rsp + c0) + i);
-        }
-    };
-    fetch(0);
+    if (0 < nq) mu_n = __ldg(reinterpret_cast<const uint4 *>(mup) + s);
 
     for (int64_t j = 0; j < nq0; ++j) {
-        // Keep the ring ahead of the reader: one step uses at most 32 V words.
-        const uint32_t need = min(nw, rp + 32u * V);
-        const uint32_t target = min(nwp4, rp + 32u * V + kBlock);
-        bool issued_extra = false;
-        while (filled < target) {
-            for (uint32_t u = lane; u < kBlock / 4; u += 32) {
-                const uint32_t w0 = filled + 4u * u;
-                if (w0 < nwp4) cp_async16(ring + (w0 & (kRing - 1)), words + w0);
-            }
-            cp_async_commit();
-            issued_extra = filled >= need;
-            filled += kBlock;
-        }
-        if (issued_extra) cp_async_wait1(); else cp_async_wait0();
-        __syncwarp();
-
         const bool active = j < nq;
-        const uint4 muv = mu_n;
-        float rsv[V];
-#pragma unroll
-        for (int i = 0; i < (int)(V / 4); ++i) {
-            rsv[4 * i + 0] = rs_n[i].x; rsv[4 * i + 1] = rs_n[i].y;
-            rsv[4 * i + 2] = rs_n[i].z; rsv[4 * i + 3] = rs_n[i].w;
-        }
-        fetch(j + 1);
+        const uint64_t q = s + (uint64_t)j * g.W;
+        const float *rse = rsp + (uint32_t)((q * V) % g.HD);
+        uint4 muv = mu_n;
+        if (j + 1 < nq) mu_n = __ldg(reinterpret_cast<const uint4 *>(mup) + q + g.W);
         uint4 outv = make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int e = 0; e < (int)V; ++e) {
+        // per-symbol inputs of the next symbol, loaded one symbol ahead
+        uint32_t mc_n = muv.x & MASK;
+        float rs_n = active ? __ldg(rse) : 1.0f;
+        uint32_t ph_n = (active && g.w_h) ? K::phat(dtab8(), a.phat, K::ord(K::finite(mc_n) ? mc_n : 0u)) : 0u;
+        // One symbol per iteration, kept rolled so the loop body stays in the
+        // instruction cache; mu codes shift out of the bottom of the vector and
+        // decoded codes shift in at the top.
+#pragma unroll 1
+        for (uint32_t e = 0; e < V; ++e) {
+            if ((e & (kStepSyms - 1u)) == 0u) {
+                // Keep the ring ahead of the reader: 8 symbols use at most 256 words.
+                const uint32_t need = min(nw, rp + 32u * kStepSyms);
+                const uint32_t target = min(nwp4, rp + 32u * kStepSyms + kBlock);
+                bool issued_extra = false;
+                while (filled < target) {
+                    const uint32_t w0 = filled + 4u * lane;
+                    if (w0 < nwp4) cp_async16(ring + (w0 & (kRing - 1)), words + w0);
+                    cp_async_commit();
+                    issued_extra = filled >= need;
+                    filled += kBlock;
+                }
+                if (issued_extra) cp_async_wait1(); else cp_async_wait0();
+                __syncwarp();
+            }
+            const uint32_t mc = mc_n;
+            const float rs = rs_n;
+            const uint32_t ph = ph_n;
+            muv.x = __funnelshift_r(muv.x, muv.y, BITS);
+            muv.y = __funnelshift_r(muv.y, muv.z, BITS);
+            muv.z = __funnelshift_r(muv.z, muv.w, BITS);
+            muv.w >>= BITS;
+            if (e + 1u < V && active) {
+                mc_n = muv.x & MASK;
+                rs_n = __ldg(rse + e + 1u);
+                if (g.w_h) ph_n = K::phat(dtab8(), a.phat, K::ord(K::finite(mc_n) ? mc_n : 0u));
+            }
+            uint32_t code = 0;
             if (active) {
-                const uint32_t mc = K::get(muv, e);
                 const bool fin = K::finite(mc);
                 bad_mu |= !fin;
                 const float mu = fin ? K::value(mc) : 0.0f;
                 const uint32_t slot = (uint32_t)x & (M - 1u);
                 uint32_t c, f;
-                const uint32_t o = find_symbol<DT>(tab, &tab8, w, a.phat, slot, mu, rsv[e],
-                                                   K::ord(mc), c, f);
+                const uint32_t o = find_symbol<DT>(a, kS, inv_total, slot, mu, rs, K::ord(fin ? mc : 0u),
+                                                   ph, c, f);
                 x = (uint64_t)f * (x >> m) + slot - c;
-                K::put(outv, e, K::code(o));
+                code = K::code(o);
             }
+            outv.x = __funnelshift_r(outv.x, outv.y, BITS);
+            outv.y = __funnelshift_r(outv.y, outv.z, BITS);
+            outv.z = __funnelshift_r(outv.z, outv.w, BITS);
+            outv.w = (outv.w >> BITS) | (code << (32u - BITS));
             const bool refill = active && x < L;
             const uint32_t ball = __ballot_sync(0xFFFFFFFFu, refill);
             if (ball) {
@@ -207,7 +417,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(const DecArgs
                 rp += __popc(ball);
             }
         }
-        if (active) reinterpret_cast<uint4 *>(outp)[s + (uint64_t)j * g.W] = outv;
+        if (active) reinterpret_cast<uint4 *>(outp)[q] = outv;
     }
     cp_async_wait0();
     corrupt |= (x != L);
@@ -219,16 +429,17 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(const DecArgs
 int launch_decode(const DecArgs &a, cudaStream_t st) {
     const uint64_t blocks = (a.n_units * a.g.G + kDecWarps - 1) / kDecWarps;
     if (blocks == 0) return 0;
-    const size_t dyn = kDecWarps * kRing * sizeof(uint32_t);
     cudaError_t e;
     if (a.g.dtype == SKV_BF16) {
-        e = cudaFuncSetAttribute(decode_kernel<SKV_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+        e = cudaFuncSetAttribute(decode_kernel<SKV_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kDecSmem);
         if (e != cudaSuccess) return 1;
-        decode_kernel<SKV_BF16><<<(unsigned)blocks, kDecWarps * 32, dyn, st>>>(a);
+        decode_kernel<SKV_BF16><<<(unsigned)blocks, kDecWarps * 32, kDecSmem, st>>>(a);
     } else {
-        e = cudaFuncSetAttribute(decode_kernel<SKV_E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+        e = cudaFuncSetAttribute(decode_kernel<SKV_E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kDecSmem);
         if (e != cudaSuccess) return 1;
-        decode_kernel<SKV_E4M3><<<(unsigned)blocks, kDecWarps * 32, dyn, st>>>(a);
+        decode_kernel<SKV_E4M3><<<(unsigned)blocks, kDecWarps * 32, kDecSmem, st>>>(a);
     }
     return cudaGetLastError() == cudaSuccess ? 0 : 1;
 }

@@ -8,7 +8,7 @@
 
 #include <cstdint>
 
-#include "../../include/skv.h"
+#include "skv.h"
 
 #define SKV_HD __host__ __device__ __forceinline__
 
@@ -107,6 +107,26 @@ struct CompactArgs {
     uint64_t out_capacity;
 };
 
+// Decoder search aids (speed only; the output does not depend on them).
+// Quantile table of the Gaussian part G of the mixture in the tail variable
+// t = -log2(g): entry i holds (z_i, z_{i+1} - z_i) with z_i = G^-1(2^-(1 + i/64)),
+// i = 0..kQuantN; t spans [1, 41], i.e. g down to 2^-41.
+constexpr uint32_t kQuantSteps = 64;
+constexpr uint32_t kQuantN = 40 * kQuantSteps;
+constexpr uint32_t kQuantFloats = 2 * (kQuantN + 1);
+
+struct QuantArgs {
+    uint32_t w_n, w_w;
+    float *qt;             // kQuantFloats: (z, dz) pairs
+};
+
+struct InvArgs {
+    Geom g;
+    const uint32_t *phat;
+    uint16_t *inv_lo;      // M entries: max{o : C_lo(o) <= s}
+    uint16_t *inv_hi;      // M entries: max{o : C_hi(o) <= s} (0 if none)
+};
+
 struct DecArgs {
     Geom g;
     const uint8_t *stream;
@@ -115,6 +135,9 @@ struct DecArgs {
     const uint8_t *mu;
     const uint32_t *phat;
     const float *rsig;
+    const float *qt;           // kQuantFloats
+    const uint16_t *inv_lo;    // NULL: found by bisection instead
+    const uint16_t *inv_hi;
     const uint32_t *ids;   // NULL: all chunks in order; else chunk ids (page mode)
     uint64_t n_units;      // chunks to decode (n_chunks or n_ids)
     uint8_t *out;          // canonical layout, or pages of page_elems codes

@@ -13,7 +13,7 @@
 
 #include <mutex>
 
-#include "../../include/skv.h"
+#include "skv.h"
 
 namespace {
 

@@ -74,8 +74,12 @@ def test_geometry_matches_oracle(dt, L, K, H, D, T, Tc, W):
                   streams_per_chunk=W)
     assert lay.n_chunks == O.num_chunks(ol)
     assert lay.max_encoded_bytes == O.max_encoded_bytes(ol)
-    assert lay.workspace_bytes(False) < (1 << 20) + 4 * L * K * H * D + 4096
-    assert lay.workspace_bytes(True) >= lay.workspace_bytes(False)
+    small = lay.workspace_bytes(False, fast=False)
+    assert small < (1 << 20) + 4 * L * K * H * D + 4096
+    m = 24 if dt == "bf16" else 16
+    assert lay.workspace_bytes(False, fast=True) == small + 2 * (2 << m)
+    if T:
+        assert lay.workspace_bytes(True) > 0
 
 
 def test_library_table_generator_is_independent_and_agrees():

@@ -167,6 +167,20 @@ def test_predictor_equal_to_target():
     assert 8.0 * s.numel() / cfg.n_elems < 0.1
 
 
+@pytest.mark.parametrize("name,kw", [("qwen3_0p6b", dict(n_layers=2, n_tokens=700)),
+                                     ("fp8_32b", dict(n_layers=2, n_tokens=300, calib_tokens=256))])
+def test_minimum_workspace_decode_is_identical(name, kw):
+    # without the outlier inverse tables far outliers are found by bisection
+    cfg = synth.CONFIGS[name].scaled(**kw)
+    wd, _ = _workload(cfg)
+    lay = H.layout_of(cfg)
+    s, offs = Coder(lay).encode(wd["kv"], wd["mu"], wd["sigma"], wd["counts"])
+    slow = Coder(lay, encode=False, fast_decode=False)
+    assert slow.workspace.numel() < lay.workspace_bytes(False, fast=True)
+    back = slow.decode(s, offs, wd["mu"], wd["sigma"], wd["counts"])
+    assert torch.equal(back, wd["kv"])
+
+
 # -------------------------------------------------------------- page access
 
 def test_decode_chunks_pages():
