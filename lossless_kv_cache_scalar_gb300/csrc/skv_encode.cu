@@ -17,6 +17,31 @@ namespace skv {
 
 constexpr int kEncWarps = 8;
 
+// Model phase for scalars [e0, e0 + 8) of a vector: (c, f) and 1/f of each.
+// No branches and no dependence on the rANS state, so the eight evaluations
+// interleave freely.
+template <uint32_t DT>
+__device__ __forceinline__ void model8(const Tables &tab, const Tables8 &tab8, const Weights w,
+                                       const uint32_t *__restrict__ phat, const uint4 &kvv,
+                                       const uint4 &muv, const float *rsv, int e0, uint32_t *cc,
+                                       uint32_t *ff, float *rf, bool &bad_mu) {
+    using K = Codes<DT>;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = e0 + i;
+        const uint32_t mc = K::get(muv, e);
+        const bool fin = K::finite(mc);
+        bad_mu |= !fin;
+        const float mu = fin ? K::value(mc) : 0.0f;
+        const uint32_t o = K::ord(K::get(kvv, e));
+        const uint32_t c = cdf<DT>(tab, &tab8, w, phat, o, mu, rsv[e]);
+        const uint32_t f = cdf<DT>(tab, &tab8, w, phat, o + 1u, mu, rsv[e]) - c;
+        cc[i] = c;
+        ff[i] = f;
+        rf[i] = recip(f);
+    }
+}
+
 template <uint32_t DT>
 __global__ void __launch_bounds__(kEncWarps * 32, 3) encode_kernel(const EncArgs a) {
     using K = Codes<DT>;
@@ -72,36 +97,35 @@ __global__ void __launch_bounds__(kEncWarps * 32, 3) encode_kernel(const EncArgs
             rsv[4 * i + 2] = rs_n[i].z; rsv[4 * i + 3] = rs_n[i].w;
         }
         fetch(j - 1);
+        // Eight scalars at a time, last eight first: model phase, then the
+        // rANS phase backwards through them.
 #pragma unroll
-        for (int e = (int)V - 1; e >= 0; --e) {
-            uint32_t c = 0, f = 1;
-            if (active) {
-                const uint32_t mc = K::get(muv, e);
-                const bool fin = K::finite(mc);
-                bad_mu |= !fin;
-                const float mu = fin ? K::value(mc) : 0.0f;
-                const uint32_t o = K::ord(K::get(kvv, e));
-                c = cdf<DT>(tab, &tab8, w, a.phat, o, mu, rsv[e]);
-                f = cdf<DT>(tab, &tab8, w, a.phat, o + 1u, mu, rsv[e]) - c;
-            }
-            const bool emit = active && (x >= ((uint64_t)f << 39));
-            const uint32_t ball = __ballot_sync(0xFFFFFFFFu, emit);
-            if (ball) {
-                const int cnt = __popc(ball);
-                if (emit) {
-                    const int64_t idx = pos - cnt + __popc(ball & lt);
-                    if (idx >= 0) slot[idx] = (uint32_t)x;
-                    else overflow = true;
-                    x >>= 32;
+        for (int h = (int)V / 8 - 1; h >= 0; --h) {
+            uint32_t cc[8], ff[8];
+            float rf[8];
+            model8<DT>(tab, tab8, w, a.phat, kvv, muv, rsv, 8 * h, cc, ff, rf, bad_mu);
+#pragma unroll
+            for (int i = 7; i >= 0; --i) {
+                const uint32_t f = active ? ff[i] : 1u;
+                const bool emit = active && (x >= ((uint64_t)f << 39));
+                const uint32_t ball = __ballot_sync(0xFFFFFFFFu, emit);
+                if (ball) {
+                    const int cnt = __popc(ball);
+                    if (emit) {
+                        const int64_t idx = pos - cnt + __popc(ball & lt);
+                        if (idx >= 0) slot[idx] = (uint32_t)x;
+                        else overflow = true;
+                        x >>= 32;
+                    }
+                    pos -= cnt;
                 }
-                pos -= cnt;
+                if (active) x = rans_put<DT>(x, cc[i], f, rf[i]);
             }
-            if (active) x = rans_put<DT>(x, c, f);
         }
     }
     a.states[gid * 32u + lane] = x;
     if (lane == 0) a.nwords[gid] = pos >= 0 ? (uint32_t)(g.cap_words - pos) : 0u;
-    if (__any_sync(0xFFFFFFFFu, bad_mu) && lane == 0) set_status(a.status, SKV_ERR_NONFINITE_MU);
+    if (__any_sync(0xFFFFFFFFu, bad_mu && nq > 0) && lane == 0) set_status(a.status, SKV_ERR_NONFINITE_MU);
     if (__any_sync(0xFFFFFFFFu, overflow) && lane == 0) set_status(a.status, SKV_ERR_CAPACITY);
 }
 

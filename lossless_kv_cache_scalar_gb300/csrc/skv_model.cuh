@@ -160,25 +160,29 @@ __device__ __forceinline__ uint32_t cdf(const Tables &t, const Tables8 *t8, cons
     z = fminf(fmaxf(z, -24.0f), 24.0f);
     const int zq = __float2int_rd(__fmul_rn(z, 65536.0f));
     const int zn = max(min(zq, 524288), -524288);
-    uint32_t S = w.n * phi_q(t.phi, zn);
-    if (w.w) {
-        // floor(zq / 3) for zq in [-3 * 2^19, 3 * 2^19]
-        const int zw = (int)(__umulhi((uint32_t)(zq + 1572864), 0xAAAAAAABu) >> 1) - 524288;
-        S += w.w * phi_q(t.phi, zw);
-    }
-    if (w.h) S += w.h * K::phat(t8, phat, o);
+    // floor(zq / 3) for zq in [-3 * 2^19, 3 * 2^19]
+    const int zw = (int)(__umulhi((uint32_t)(zq + 1572864), 0xAAAAAAABu) >> 1) - 524288;
+    // branch-free: a zero weight multiplies its term away (P_hat is all zeros
+    // when its weight is 0), so one straight-line block serves every mixture
+    const uint32_t S = w.n * phi_q(t.phi, zn) + w.w * phi_q(t.phi, zw) + w.h * K::phat(t8, phat, o);
     const uint64_t prod = (uint64_t)S * MN;
     return o + (uint32_t)(prod >> 24) / 100u;
 }
 
 // ------------------------------------------------------------------- rANS
 
-// q = floor(x / f), r = x mod f for f in [1, 2^24] and x < 2^39 f.
-// A binary32 reciprocal estimate gives q to within 2^17 + 1; one more estimate
-// on the signed remainder lands within one step, fixed by a final compare.
-__device__ __forceinline__ uint64_t divmod(uint64_t x, uint32_t f, uint32_t &r_out) {
+// Approximate reciprocal of f (one MUFU op), computed off the state chain.
+__device__ __forceinline__ float recip(uint32_t f) {
     float rf;
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rf) : "f"(__uint2float_rn(f)));
+    return rf;
+}
+
+// q = floor(x / f), r = x mod f for f in [1, 2^24] and x < 2^39 f, given
+// rf = recip(f) (relative error below 2^-22). The binary32 estimate gives q to
+// within 2^17 + 1; one more estimate on the signed remainder lands within one
+// step, fixed by a final compare.
+__device__ __forceinline__ uint64_t divmod(uint64_t x, uint32_t f, float rf, uint32_t &r_out) {
     const uint64_t q1 = __float2ull_rz(__fmul_rn(__ull2float_rn(x), rf));
     long long r = (long long)(x - q1 * (uint64_t)f);
     const int q2 = __float2int_rn(__fmul_rn(__ll2float_rn(r), rf));
@@ -191,9 +195,9 @@ __device__ __forceinline__ uint64_t divmod(uint64_t x, uint32_t f, uint32_t &r_o
 
 // Encode one symbol after renormalisation: x = (x / f) M + (x mod f) + c.
 template <uint32_t DT>
-__device__ __forceinline__ uint64_t rans_put(uint64_t x, uint32_t c, uint32_t f) {
+__device__ __forceinline__ uint64_t rans_put(uint64_t x, uint32_t c, uint32_t f, float rf) {
     uint32_t r;
-    const uint64_t q = divmod(x, f, r);
+    const uint64_t q = divmod(x, f, rf, r);
     return (q << Codes<DT>::m) + r + c;
 }
 
