@@ -290,7 +290,7 @@ def main():
             "roofline_decode_frac": ALG_OPS[(lay.dtype, "decode")] * n_el / (t_dec / args.steps) / 1e12 / peak_tops,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 6 * args.steps,
+            "gpu_launches": 8 * args.steps,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
