@@ -20,9 +20,8 @@
 // mu's own code, a second at the first estimate. A far outlier that only
 // p_hat explains (both Gaussians saturated, so C is a mu-independent function
 // of o) is read from per-call inverse tables instead. When the test fails,
-// Newton steps in code space (using each probe's own code width) inside a
-// shrinking bracket, then bisection, find the code. Search aids change speed
-// only; the decoded codes are fixed by the exact test.
+// the whole warp searches for that lane's code together (cooperative_search).
+// Search aids change speed only; the decoded codes are fixed by the exact test.
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
@@ -178,45 +177,52 @@ __device__ __forceinline__ uint32_t estimate(const DecArgs &a, float kS, float i
     return nearest_ord<DT>(fmaf(below ? zt : -zt, sigma, mu));
 }
 
-// The slow path: the estimate o failed (C(o) = clo, C(o+1) = chi). Newton
-// steps in code space, o += (s - C(o)) / f(o), using each probe's own width,
-// inside a bracket [lo, hi) with C(lo) <= s < C(hi) that every probe narrows;
-// then bisection of whatever bracket is left. Near zero, where bf16 codes are
-// dense and each owns about one slot, and in the tails, a step lands within a
-// few codes where the estimate in z could be thousands of codes off.
+// The slow path, run by the whole warp for one lane whose estimate failed.
+// Lane L's slot sL, mu and 1/sigma are broadcast; each round the 32 lanes
+// evaluate C at 32 ascending candidates inside the bracket [lo, hi) (C(lo) <=
+// sL < C(hi), both known) and a ballot finds the sub-interval holding sL. The
+// first round spreads the candidates geometrically away from the failed
+// estimate (1, 2, 4, ... codes), so a near miss ends at once and a far one is
+// bracketed within a factor of two; later rounds split the bracket 33 ways.
+// No 16-bit code space needs more than four rounds after the first.
 template <uint32_t DT>
-__device__ __noinline__ uint32_t find_fallback(const DecArgs &a, uint32_t s, float mu, float rs,
-                                               uint32_t o, uint32_t clo, uint32_t chi,
-                                               uint32_t &c_out, uint32_t &f_out) {
+__device__ __forceinline__ void cooperative_search(const DecArgs &a, uint32_t L, uint32_t s, float mu,
+                                                float rs, uint32_t o, uint32_t clo, uint32_t chi,
+                                                uint32_t &o_out, uint32_t &c_out, uint32_t &f_out) {
     using K = Codes<DT>;
     constexpr uint32_t M = 1u << K::m;
-    const Tables &t = dtab();
-    const Tables8 *t8 = dtab8();
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t sL = __shfl_sync(0xFFFFFFFFu, s, L);
+    const float muL = __shfl_sync(0xFFFFFFFFu, mu, L);
+    const float rsL = __shfl_sync(0xFFFFFFFFu, rs, L);
+    const uint32_t oL = __shfl_sync(0xFFFFFFFFu, o, L);
+    const uint32_t cloL = __shfl_sync(0xFFFFFFFFu, clo, L);
+    const uint32_t chiL = __shfl_sync(0xFFFFFFFFu, chi, L);
+    const bool down = sL < cloL;
+    uint32_t lo, hi, Clo, Chi;
+    if (down) { lo = 0; Clo = 0; hi = oL; Chi = cloL; }
+    else { lo = oL + 1u; Clo = chiL; hi = K::N; Chi = M; }
     const Weights w{a.g.w_n, a.g.w_w, a.g.w_h};
-    // bracket: C(lo) <= s < C(hi); Clo/Chi are C there when known
-    uint32_t lo = 0, hi = K::N, Clo = 0, Chi = M;
-    if (s < clo) { hi = o; Chi = clo; } else { lo = o + 1u; Clo = chi; }
-    uint32_t oc = o, cc = clo, fc = chi - clo;
-    for (int it = 0; it < 6 && hi - lo > 1u; ++it) {
-        // Newton step from (oc, C(oc), f(oc)), kept strictly inside the bracket
-        const float step = ((float)s - (float)cc) / (float)fc;
-        const float fo = fminf(fmaxf((float)oc + floorf(step), (float)lo), (float)(hi - 1u));
-        const uint32_t cand = (uint32_t)fo;
-        const uint32_t ca = (cand == lo && lo == o + 1u) ? chi : cdf<DT>(t, t8, w, a.phat, cand, mu, rs);
-        const uint32_t cb = (cand + 1u == hi) ? Chi : cdf<DT>(t, t8, w, a.phat, cand + 1u, mu, rs);
-        if (ca <= s && s < cb) { c_out = ca; f_out = cb - ca; return cand; }
-        if (s < ca) { hi = cand; Chi = ca; } else { lo = cand + 1u; Clo = cb; }
-        oc = cand; cc = ca; fc = cb - ca;
+    for (int round = 0; hi - lo > 1u; ++round) {
+        const uint32_t span = hi - lo;
+        uint32_t cand;
+        if (round == 0) {
+            // 1, 2, 4, ... codes away from the estimate, ascending with the lane
+            cand = down ? hi - min(1u << (31u - lane), span - 1u) : lo + min(1u << lane, span - 1u);
+        } else {
+            cand = lo + 1u + (uint32_t)(((uint64_t)(span - 1u) * lane) / 32u);
+        }
+        const uint32_t c = cdf<DT>(dtab(), dtab8(), w, a.phat, cand, muL, rsL);
+        const uint32_t le = __ballot_sync(0xFFFFFFFFu, c <= sL);   // a prefix of the lanes
+        const uint32_t k = __popc(le);
+        const uint32_t c_lo = __shfl_sync(0xFFFFFFFFu, c, k ? k - 1u : 0u);
+        const uint32_t o_lo = __shfl_sync(0xFFFFFFFFu, cand, k ? k - 1u : 0u);
+        const uint32_t c_hi = __shfl_sync(0xFFFFFFFFu, c, k < 32u ? k : 31u);
+        const uint32_t o_hi = __shfl_sync(0xFFFFFFFFu, cand, k < 32u ? k : 31u);
+        if (k > 0u && o_lo > lo) { lo = o_lo; Clo = c_lo; }
+        if (k < 32u && o_hi < hi) { hi = o_hi; Chi = c_hi; }
     }
-    // bisection on what is left
-    while (hi - lo > 1u) {
-        const uint32_t mid = (lo + hi) >> 1;
-        const uint32_t cm = cdf<DT>(t, t8, w, a.phat, mid, mu, rs);
-        if (cm <= s) { lo = mid; Clo = cm; } else { hi = mid; Chi = cm; }
-    }
-    c_out = Clo;
-    f_out = Chi - Clo;
-    return lo;
+    if (lane == L) { o_out = lo; c_out = Clo; f_out = Chi - Clo; }
 }
 
 // max{o < N : C_sat(o) <= s} from the per-call table, or by bisection without it.
@@ -226,7 +232,8 @@ __device__ __forceinline__ uint32_t saturated_inverse(const DecArgs &a, uint32_t
     return tab ? (uint32_t)__ldg(tab + s) : sat_search<DT>(s, base, a.g.w_h, a.phat, 0u, Codes<DT>::N);
 }
 
-// The code o with C(o) <= s < C(o+1), and (c, f) = (C(o), C(o+1) - C(o)).
+// The estimated code o for slot s, with c = C(o) and C(o+1) - C(o) in f; the
+// caller checks C(o) <= s < C(o+1) and resolves misses cooperatively.
 template <uint32_t DT>
 __device__ __forceinline__ uint32_t find_symbol(const DecArgs &a, float kS, float inv_total,
                                                 uint32_t s, float mu, float rs, uint32_t o_mu,
@@ -248,12 +255,9 @@ __device__ __forceinline__ uint32_t find_symbol(const DecArgs &a, float kS, floa
     if (far) o = saturated_inverse<DT>(a, s, (below || !(w.n + w.w)) ? 0u : (w.n + w.w) << 24);
     const uint32_t clo = cdf<DT>(dtab(), dtab8(), w, a.phat, o, mu, rs);
     const uint32_t chi = cdf<DT>(dtab(), dtab8(), w, a.phat, o + 1u, mu, rs);
-    if (clo <= s && s < chi) {
-        c_out = clo;
-        f_out = chi - clo;
-        return o;
-    }
-    return find_fallback<DT>(a, s, mu, rs, o, clo, chi, c_out, f_out);
+    c_out = clo;
+    f_out = chi - clo;
+    return o;
 }
 
 // ----------------------------------------------------------------- kernel
@@ -388,15 +392,25 @@ __global__ void __launch_bounds__(kDecWarps * 32, 3) decode_kernel(const DecArgs
                 rs_n = __ldg(rse + e + 1u);
                 if (g.w_h) ph_n = K::phat(dtab8(), a.phat, K::ord(K::finite(mc_n) ? mc_n : 0u));
             }
-            uint32_t code = 0;
+            uint32_t code = 0, slot = 0, o = 0, c = 0, f = 1;
+            float mu = 0.0f;
+            bool miss = false;
             if (active) {
                 const bool fin = K::finite(mc);
                 bad_mu |= !fin;
-                const float mu = fin ? K::value(mc) : 0.0f;
-                const uint32_t slot = (uint32_t)x & (M - 1u);
-                uint32_t c, f;
-                const uint32_t o = find_symbol<DT>(a, kS, inv_total, slot, mu, rs, K::ord(fin ? mc : 0u),
-                                                   ph, c, f);
+                mu = fin ? K::value(mc) : 0.0f;
+                slot = (uint32_t)x & (M - 1u);
+                o = find_symbol<DT>(a, kS, inv_total, slot, mu, rs, K::ord(fin ? mc : 0u), ph, c, f);
+                miss = !(c <= slot && slot - c < f);
+            }
+            // misses are resolved by the whole warp, one lane at a time
+            uint32_t pending = __ballot_sync(0xFFFFFFFFu, miss);
+            while (pending) {
+                const uint32_t Lm = __ffs(pending) - 1u;
+                pending &= pending - 1u;
+                cooperative_search<DT>(a, Lm, slot, mu, rs, o, c, c + f, o, c, f);
+            }
+            if (active) {
                 x = (uint64_t)f * (x >> m) + slot - c;
                 code = K::code(o);
             }
