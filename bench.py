@@ -140,7 +140,7 @@ def run_reference(args, cfg):
     gbs = total_b / total_t / 1e9
     line = {"metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32+f32",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32/u64 int + f32",
             "data": "synthetic", "impl": "reference",
             "config": {"workload": cfg.name, "sample": desc},
             "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
