@@ -50,7 +50,10 @@ __global__ void __launch_bounds__(1024) setup_kernel(const SetupArgs a) {
     }
 
     if (g.w_h == 0) {
-        for (uint32_t o = tid; o <= K::N; o += blockDim.x) a.phat[o] = 0u;
+        for (uint32_t o = tid; o <= K::N; o += blockDim.x) {
+            a.phat[o] = 0u;
+            if (DT == SKV_BF16 && a.ep) a.ep[o] = make_uint2(__float_as_uint(K::edge(nullptr, o)), 0u);
+        }
     } else {
         constexpr uint32_t per = (K::N + 1023u) / 1024u;
         const uint32_t o0 = tid * per, o1 = min(o0 + per, K::N);
@@ -78,14 +81,22 @@ __global__ void __launch_bounds__(1024) setup_kernel(const SetupArgs a) {
         const uint64_t total = warp_tot[31];
         uint64_t cum = (warp ? warp_tot[warp - 1] : 0ull) + incl - local;
         if (total == 0) {
-            for (uint32_t o = tid; o <= K::N; o += blockDim.x) a.phat[o] = 0u;
+            for (uint32_t o = tid; o <= K::N; o += blockDim.x) {
+                a.phat[o] = 0u;
+                if (DT == SKV_BF16 && a.ep) a.ep[o] = make_uint2(__float_as_uint(K::edge(nullptr, o)), 0u);
+            }
             if (tid == 0) set_status(a.status, SKV_ERR_EMPTY_MARGINAL);
         } else {
             for (uint32_t o = o0; o < o1; ++o) {
-                a.phat[o] = phat_entry(cum, total);
+                const uint32_t p = phat_entry(cum, total);
+                a.phat[o] = p;
+                if (DT == SKV_BF16 && a.ep) a.ep[o] = make_uint2(__float_as_uint(K::edge(nullptr, o)), p);
                 cum += a.counts[K::code(o)];
             }
-            if (tid == 0) a.phat[K::N] = 1u << 24;
+            if (tid == 0) {
+                a.phat[K::N] = 1u << 24;
+                if (DT == SKV_BF16 && a.ep) a.ep[K::N] = make_uint2(__float_as_uint(K::edge(nullptr, K::N)), 1u << 24);
+            }
         }
     }
     __syncthreads();
@@ -171,6 +182,7 @@ static uint64_t chunk_max_bytes(const Geom &g, uint64_t n_vec) {
 }
 
 struct Workspace {
+    uint2 *ep;
     uint32_t *phat;
     float *rsig;
     float *qt;
@@ -196,6 +208,11 @@ static Workspace carve(const Geom &g, int kind, uint8_t *base) {
     off += round256(4ull * (d.N + 1));
     o_rsig = off;
     off += round256(4ull * g.n_planes * g.HD);
+    uint64_t o_ep = 0;
+    if (kind == WS_ENCODE && g.dtype == SKV_BF16) {
+        o_ep = off;
+        off += round256(8ull * (d.N + 1));
+    }
     if (kind == WS_ENCODE) {
         o_states = off;
         off += round256(8ull * 32ull * g.n_groups);
@@ -219,6 +236,7 @@ static Workspace carve(const Geom &g, int kind, uint8_t *base) {
         w.phat = reinterpret_cast<uint32_t *>(base + o_phat);
         w.rsig = reinterpret_cast<float *>(base + o_rsig);
         if (kind == WS_ENCODE) {
+            if (g.dtype == SKV_BF16) w.ep = reinterpret_cast<uint2 *>(base + o_ep);
             w.states = reinterpret_cast<uint64_t *>(base + o_states);
             w.nwords = reinterpret_cast<uint32_t *>(base + o_nwords);
             w.scratch = reinterpret_cast<uint32_t *>(base + o_scratch);
@@ -235,7 +253,7 @@ static Workspace carve(const Geom &g, int kind, uint8_t *base) {
 
 static int32_t run_setup(const Geom &g, const float *sigma, const uint64_t *counts,
                          const Workspace &ws, int32_t *status, cudaStream_t st) {
-    SetupArgs s{g, sigma, counts, ws.phat, ws.rsig, status};
+    SetupArgs s{g, sigma, counts, ws.phat, ws.rsig, ws.ep, status};
     if (g.dtype == SKV_BF16) setup_kernel<SKV_BF16><<<1, 1024, 0, st>>>(s);
     else setup_kernel<SKV_E4M3><<<1, 1024, 0, st>>>(s);
     return cudaGetLastError() == cudaSuccess ? SKV_OK : SKV_ERR_CUDA;
@@ -340,7 +358,7 @@ int32_t skv_encode(const skv_layout *lay, const void *kv, const void *mu, const 
     const Workspace ws = carve(g, WS_ENCODE, static_cast<uint8_t *>(workspace));
     if ((r = run_setup(g, sigma, counts, ws, status, st)) != SKV_OK) return r;
     EncArgs ea{g, static_cast<const uint8_t *>(kv), static_cast<const uint8_t *>(mu), ws.phat,
-               ws.rsig, ws.states, ws.nwords, ws.scratch, status};
+               ws.ep, ws.rsig, ws.states, ws.nwords, ws.scratch, status};
     if (launch_encode(ea, st)) return SKV_ERR_CUDA;
     ScanArgs sa{g, ws.nwords, offsets, out_capacity, status};
     if (launch_scan(sa, st)) return SKV_ERR_CUDA;
@@ -413,7 +431,7 @@ int32_t skv_cdf_eval(const skv_layout *lay, const uint64_t *counts, uint64_t n,
     // P_hat only; sigma is per query here, so rsig is not built
     Geom g1 = g;
     g1.n_planes = 0;
-    SetupArgs s{g1, nullptr, counts, ws.phat, ws.rsig, status};
+    SetupArgs s{g1, nullptr, counts, ws.phat, ws.rsig, nullptr, status};
     if (g.dtype == SKV_BF16) setup_kernel<SKV_BF16><<<1, 1024, 0, st>>>(s);
     else setup_kernel<SKV_E4M3><<<1, 1024, 0, st>>>(s);
     if (cudaGetLastError() != cudaSuccess) return SKV_ERR_CUDA;

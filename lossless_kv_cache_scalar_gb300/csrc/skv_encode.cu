@@ -22,7 +22,8 @@ constexpr int kEncWarps = 8;
 // interleave freely.
 template <uint32_t DT>
 __device__ __forceinline__ void model8(const Tables &tab, const Tables8 &tab8, const Weights w,
-                                       const uint32_t *__restrict__ phat, const uint4 &kvv,
+                                       const uint32_t *__restrict__ phat, const uint2 *__restrict__ ep,
+                                       const uint4 &kvv,
                                        const uint4 &muv, const float *rsv, int e0, uint32_t *cc,
                                        uint32_t *ff, float *rf, bool &bad_mu) {
     using K = Codes<DT>;
@@ -34,8 +35,14 @@ __device__ __forceinline__ void model8(const Tables &tab, const Tables8 &tab8, c
         bad_mu |= !fin;
         const float mu = fin ? K::value(mc) : 0.0f;
         const uint32_t o = K::ord(K::get(kvv, e));
-        const uint32_t c = cdf<DT>(tab, &tab8, w, phat, o, mu, rsv[e]);
-        const uint32_t f = cdf<DT>(tab, &tab8, w, phat, o + 1u, mu, rsv[e]) - c;
+        uint32_t c, f;
+        if (DT == SKV_BF16) {
+            c = cdf_ep(tab, w, ep, o, mu, rsv[e]);
+            f = cdf_ep(tab, w, ep, o + 1u, mu, rsv[e]) - c;
+        } else {
+            c = cdf<DT>(tab, &tab8, w, phat, o, mu, rsv[e]);
+            f = cdf<DT>(tab, &tab8, w, phat, o + 1u, mu, rsv[e]) - c;
+        }
         cc[i] = c;
         ff[i] = f;
         rf[i] = recip(f);
@@ -103,7 +110,7 @@ __global__ void __launch_bounds__(kEncWarps * 32, 3) encode_kernel(const EncArgs
         for (int h = (int)V / 8 - 1; h >= 0; --h) {
             uint32_t cc[8], ff[8];
             float rf[8];
-            model8<DT>(tab, tab8, w, a.phat, kvv, muv, rsv, 8 * h, cc, ff, rf, bad_mu);
+            model8<DT>(tab, tab8, w, a.phat, a.ep, kvv, muv, rsv, 8 * h, cc, ff, rf, bad_mu);
 #pragma unroll
             for (int i = 7; i >= 0; --i) {
                 const uint32_t f = active ? ff[i] : 1u;

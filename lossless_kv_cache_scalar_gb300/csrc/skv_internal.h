@@ -74,6 +74,7 @@ struct SetupArgs {
     const uint64_t *counts;
     uint32_t *phat;        // N + 1 entries
     float *rsig;           // n_planes * HD
+    uint2 *ep;             // bf16 encode only (else NULL): (edge bits, P_hat) per ordinal, N + 1
     int32_t *status;
 };
 
@@ -82,6 +83,7 @@ struct EncArgs {
     const uint8_t *kv;
     const uint8_t *mu;
     const uint32_t *phat;
+    const uint2 *ep;       // bf16: (edge bits, P_hat) per ordinal
     const float *rsig;
     uint64_t *states;      // n_groups * 32
     uint32_t *nwords;      // n_groups

@@ -169,6 +169,26 @@ __device__ __forceinline__ uint32_t cdf(const Tables &t, const Tables8 *t8, cons
     return o + (uint32_t)(prod >> 24) / 100u;
 }
 
+// C(o) as cdf<SKV_BF16>, with the edge E(o) and P_hat(o) read as one pair
+// from the per-call table ep (ep[o] = (bits of E(o), P_hat(o))) instead of
+// being rebuilt from the code bits: one 8-byte load replaces the edge's
+// integer work and the P_hat load.
+__device__ __forceinline__ uint32_t cdf_ep(const Tables &t, const Weights w,
+                                           const uint2 *__restrict__ ep, uint32_t o, float mu,
+                                           float rs) {
+    constexpr uint32_t MN = (1u << 24) - 65536u;
+    const uint2 e = __ldg(ep + o);
+    const float d = __fsub_rn(__uint_as_float(e.x), mu);
+    float z = __fmul_rn(d, rs);
+    z = fminf(fmaxf(z, -24.0f), 24.0f);
+    const int zq = __float2int_rd(__fmul_rn(z, 65536.0f));
+    const int zn = max(min(zq, 524288), -524288);
+    const int zw = (int)(__umulhi((uint32_t)(zq + 1572864), 0xAAAAAAABu) >> 1) - 524288;
+    const uint32_t S = w.n * phi_q(t.phi, zn) + w.w * phi_q(t.phi, zw) + w.h * e.y;
+    const uint64_t prod = (uint64_t)S * MN;
+    return o + (uint32_t)(prod >> 24) / 100u;
+}
+
 // ------------------------------------------------------------------- rANS
 
 // Approximate reciprocal of f (one MUFU op), computed off the state chain.
