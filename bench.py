@@ -165,7 +165,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     ap.add_argument("--layers", type=int, default=None, help="override n_layers (profiling cases)")
+    ap.add_argument("--streams", type=int, default=64, help="streams per chunk (32..256)")
     ap.add_argument("--tokens", type=int, default=None, help="override n_tokens (profiling cases)")
+    ap.add_argument("--page-latency", type=int, default=200,
+                    help="single-page random decodes timed after the run (0: skip)")
     ap.add_argument("--traffic-json", default=os.path.join(ROOT, "profiles", "traffic.json"))
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "skv" else args.warmup
@@ -186,7 +189,8 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     cfg = cfg.scaled(seed=cfg.seed + 1000 * rank) if world > 1 else cfg
     w = synth.generate(cfg, device=dev)
-    lay = skv.Layout(cfg.dtype, cfg.n_layers, cfg.n_kv, cfg.n_heads, cfg.head_dim, cfg.n_tokens)
+    lay = skv.Layout(cfg.dtype, cfg.n_layers, cfg.n_kv, cfg.n_heads, cfg.head_dim, cfg.n_tokens,
+                     streams_per_chunk=args.streams)
     coder = skv.Coder(lay, dev)
     out, offsets = coder.alloc_output()
     back = torch.empty_like(w["mu"])
@@ -250,6 +254,7 @@ def main():
     except (OSError, ValueError):
         traffic = None
     hbm_peak = _peaks().get("hbm_gbs", 6685.5)
+    page_lat = page_latency(coder, out, offsets, w, lay, args, dev) if args.page_latency else None
     bits = 8.0 * total_bytes / n_el
 
     # end to end through the public API with host buffers
@@ -289,6 +294,7 @@ def main():
             "roofline_encode_frac": ALG_OPS[(lay.dtype, "encode")] * n_el / (t_enc / args.steps) / 1e12 / peak_tops,
             "roofline_decode_frac": ALG_OPS[(lay.dtype, "decode")] * n_el / (t_dec / args.steps) / 1e12 / peak_tops,
             "cpu_baseline": cpu,
+            "page_decode_latency_us": page_lat,
             "e2e": e2e,
             "gpu_launches": 8 * args.steps,
             "clocks": clocks,
@@ -299,6 +305,32 @@ def main():
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def page_latency(coder, out, offsets, w, lay, args, dev):
+    """Random single-page decodes after a one-time skv_decode_prepare: per-call
+    device time (CUDA events around each call, same stream), p50/p99 in us."""
+    stream = torch.cuda.Stream(device=dev)
+    rng = np.random.default_rng(7)
+    ids = rng.integers(0, lay.n_chunks, args.page_latency)
+    page = torch.empty(lay.page_elems, dtype=w["mu"].dtype, device=dev)
+    idt = torch.tensor(ids, dtype=torch.int32, device=dev)
+    with torch.cuda.stream(stream):
+        coder.prepare_decode(w["sigma"], w["counts"], stream)
+        for i in range(min(5, len(ids))):       # warm-up
+            coder.decode_chunks_prepared_into(out, offsets, w["mu"], idt[i:i + 1], page, stream)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ids]
+        for i, (e0, e1) in enumerate(evs):
+            e0.record(stream)
+            coder.decode_chunks_prepared_into(out, offsets, w["mu"], idt[i:i + 1], page, stream)
+            e1.record(stream)
+    stream.synchronize()
+    coder.check_status("page latency", stream)
+    t = np.array([e0.elapsed_time(e1) * 1e3 for e0, e1 in evs])
+    return {"p50": float(np.percentile(t, 50)), "p99": float(np.percentile(t, 99)),
+            "pages": int(len(ids)), "page_scalars": lay.page_elems,
+            "streams_per_chunk": lay.streams_per_chunk,
+            "note": "one 256-token page per skv_decode_chunks_prepared call, tables prepared once"}
 
 
 def e2e_run(coder, w, lay, args, dev, total_bytes):

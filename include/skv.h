@@ -182,6 +182,28 @@ int32_t skv_decode_chunks(const skv_layout *lay, const void *bitstream, uint64_t
                           void *stream);
 
 /*
+ * Random access without per-call set-up. skv_decode_prepare builds the
+ * decoder's tables (P_hat, 1/sigma, quantile and, with a workspace of
+ * skv_workspace_bytes(lay, 2), the outlier inverse tables) into the workspace
+ * once; skv_decode_chunks_prepared then decodes pages exactly as
+ * skv_decode_chunks does, reading those tables, for as many calls as the
+ * tables stay valid: the same layout, sigma, counts, workspace and ws_bytes,
+ * and no other call using that workspace in between. This serves the page
+ * access the wiki's uses section describes (offload, long context), where a
+ * few pages are wanted at a time and the set-up would dominate.
+ * skv_decode_prepare writes BAD_SIGMA / EMPTY_MARGINAL to *status; check it
+ * before decoding (the decode call resets *status). Arguments as in
+ * skv_decode_chunks; the workspace is only read by the decode call.
+ */
+int32_t skv_decode_prepare(const skv_layout *lay, const float *sigma, const uint64_t *counts,
+                           int32_t *status, void *workspace, uint64_t ws_bytes, void *stream);
+int32_t skv_decode_chunks_prepared(const skv_layout *lay, const void *bitstream,
+                                   uint64_t bitstream_bytes, const uint64_t *offsets, const void *mu,
+                                   const uint32_t *chunk_ids, uint32_t n_ids, void *pages_out,
+                                   int32_t *status, const void *workspace, uint64_t ws_bytes,
+                                   void *stream);
+
+/*
  * Evaluate the model's cumulative frequency C(o) (FORMAT.md section 5) for n
  * independent queries: C[i] = C(ords[i]) for predictor code mu_codes[i] and
  * scale sigmas[i], under the weights of lay and the marginal counts. For

@@ -43,6 +43,8 @@ SIGNATURES = {
                                  _u64, _vp]),
     "skv_cdf_eval": (_i32, [_LP, _vp, _u64, _vp, _vp, _vp, _vp, _vp, _vp, _u64, _vp]),
     "skv_decode_noalloc": (_i32, [_LP, _vp, _u64, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "skv_decode_prepare": (_i32, [_LP, _vp, _vp, _vp, _vp, _u64, _vp]),
+    "skv_decode_chunks_prepared": (_i32, [_LP, _vp, _u64, _vp, _vp, _vp, _u32, _vp, _vp, _vp, _u64, _vp]),
 }
 
 _lib = None

@@ -180,6 +180,28 @@ class Coder:
                                        _stream_handle(stream))
         B.check("skv_decode_chunks", rc)
 
+    def prepare_decode(self, sigma, counts, stream=None, check: bool = True):
+        """Build the decoder tables once (skv_decode_prepare) for decode_chunks_prepared."""
+        rc = B.lib().skv_decode_prepare(C.byref(self._c), _ptr(sigma), _ptr(counts), _ptr(self.status),
+                                        _ptr(self.workspace), self.workspace.numel(),
+                                        _stream_handle(stream))
+        B.check("skv_decode_prepare", rc)
+        if check:
+            self.check_status("skv_decode_prepare", stream)
+
+    def decode_chunks_prepared_into(self, bitstream, offsets, mu, chunk_ids, pages_out, stream=None):
+        lay = self.layout
+        if chunk_ids.dtype != torch.int32 or not chunk_ids.is_cuda:
+            raise ValueError("chunk_ids must be an int32 CUDA tensor")
+        if pages_out.numel() != chunk_ids.numel() * lay.page_elems:
+            raise ValueError("pages_out must hold n_ids * tokens_per_chunk * HD codes")
+        rc = B.lib().skv_decode_chunks_prepared(C.byref(self._c), _ptr(bitstream), bitstream.numel(),
+                                                _ptr(offsets), _ptr(mu), _ptr(chunk_ids),
+                                                chunk_ids.numel(), _ptr(pages_out), _ptr(self.status),
+                                                _ptr(self.workspace), self.workspace.numel(),
+                                                _stream_handle(stream))
+        B.check("skv_decode_chunks_prepared", rc)
+
     def decode_chunks(self, bitstream, offsets, mu, sigma, counts, chunk_ids, stream=None):
         lay = self.layout
         pages = torch.zeros((chunk_ids.numel(), lay.page_elems), dtype=mu.dtype, device=mu.device)

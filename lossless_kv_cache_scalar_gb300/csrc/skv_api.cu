@@ -368,6 +368,40 @@ int32_t skv_encode(const skv_layout *lay, const void *kv, const void *mu, const 
     return SKV_OK;
 }
 
+// Decoder tables (P_hat, 1/sigma, quantiles, and with a full workspace the
+// outlier inverse tables) built on the stream into the workspace.
+static int32_t decode_tables(const Geom &g, const float *sigma, const uint64_t *counts,
+                             int32_t *status, void *workspace, uint64_t ws_bytes, cudaStream_t st,
+                             Workspace &ws) {
+    const int kind = ws_bytes >= carve(g, WS_DECODE_FULL, nullptr).bytes ? WS_DECODE_FULL : WS_DECODE_MIN;
+    ws = carve(g, kind, static_cast<uint8_t *>(workspace));
+    const int32_t r = run_setup(g, sigma, counts, ws, status, st);
+    if (r != SKV_OK) return r;
+    if (launch_search_aids(g, ws.phat, ws.qt, ws.inv_lo, ws.inv_hi, st)) return SKV_ERR_CUDA;
+    return SKV_OK;
+}
+
+static int32_t decode_launch(const Geom &g, const void *bitstream, uint64_t bitstream_bytes,
+                             const uint64_t *offsets, const void *mu, const uint32_t *ids,
+                             uint64_t n_units, bool pages, void *out, int32_t *status,
+                             const Workspace &ws, cudaStream_t st) {
+    if (n_units == 0) return SKV_OK;
+    DecArgs da{g, static_cast<const uint8_t *>(bitstream), bitstream_bytes, offsets,
+               static_cast<const uint8_t *>(mu), ws.phat, ws.rsig, ws.qt, ws.inv_lo, ws.inv_hi,
+               pages ? ids : nullptr,
+               n_units, static_cast<uint8_t *>(out), (uint64_t)g.Tc * g.HD, status};
+    return launch_decode(da, st) ? SKV_ERR_CUDA : SKV_OK;
+}
+
+static int32_t decode_args_check(const Geom &g, const void *bitstream, const uint64_t *offsets,
+                                 const void *mu, const uint32_t *ids, uint64_t n_units, bool pages,
+                                 void *out) {
+    if (n_units && (!bitstream || !offsets || !mu || !out)) return SKV_ERR_INVALID_ARG;
+    if (pages && n_units && !ids) return SKV_ERR_INVALID_ARG;
+    if (n_units && (!aligned16(bitstream) || !aligned16(mu) || !aligned16(out))) return SKV_ERR_INVALID_ARG;
+    return SKV_OK;
+}
+
 static int32_t decode_impl(const skv_layout *lay, const void *bitstream, uint64_t bitstream_bytes,
                            const uint64_t *offsets, const void *mu, const float *sigma,
                            const uint64_t *counts, const uint32_t *ids, uint64_t n_units,
@@ -379,22 +413,13 @@ static int32_t decode_impl(const skv_layout *lay, const void *bitstream, uint64_
     r = common_checks(g, sigma, counts, status, workspace, ws_bytes, WS_DECODE_MIN);
     if (r != SKV_OK) return r;
     if (!pages) n_units = g.n_chunks;
-    if (n_units && (!bitstream || !offsets || !mu || !out)) return SKV_ERR_INVALID_ARG;
-    if (pages && n_units && !ids) return SKV_ERR_INVALID_ARG;
-    if (n_units && (!aligned16(bitstream) || !aligned16(mu) || !aligned16(out))) return SKV_ERR_INVALID_ARG;
+    if ((r = decode_args_check(g, bitstream, offsets, mu, ids, n_units, pages, out)) != SKV_OK) return r;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return SKV_ERR_CUDA;
-    const int kind = ws_bytes >= carve(g, WS_DECODE_FULL, nullptr).bytes ? WS_DECODE_FULL : WS_DECODE_MIN;
-    const Workspace ws = carve(g, kind, static_cast<uint8_t *>(workspace));
-    if ((r = run_setup(g, sigma, counts, ws, status, st)) != SKV_OK) return r;
-    if (n_units == 0) return SKV_OK;
-    if (launch_search_aids(g, ws.phat, ws.qt, ws.inv_lo, ws.inv_hi, st)) return SKV_ERR_CUDA;
-    DecArgs da{g, static_cast<const uint8_t *>(bitstream), bitstream_bytes, offsets,
-               static_cast<const uint8_t *>(mu), ws.phat, ws.rsig, ws.qt, ws.inv_lo, ws.inv_hi,
-               pages ? ids : nullptr,
-               n_units, static_cast<uint8_t *>(out), (uint64_t)g.Tc * g.HD, status};
-    if (launch_decode(da, st)) return SKV_ERR_CUDA;
-    return SKV_OK;
+    Workspace ws;
+    if ((r = decode_tables(g, sigma, counts, status, workspace, ws_bytes, st, ws)) != SKV_OK) return r;
+    return decode_launch(g, bitstream, bitstream_bytes, offsets, mu, ids, n_units, pages, out, status,
+                         ws, st);
 }
 
 int32_t skv_decode(const skv_layout *lay, const void *bitstream, uint64_t bitstream_bytes,
@@ -412,6 +437,39 @@ int32_t skv_decode_chunks(const skv_layout *lay, const void *bitstream, uint64_t
                           void *stream) {
     return decode_impl(lay, bitstream, bitstream_bytes, offsets, mu, sigma, counts, chunk_ids,
                        n_ids, true, pages_out, status, workspace, ws_bytes, stream);
+}
+
+int32_t skv_decode_prepare(const skv_layout *lay, const float *sigma, const uint64_t *counts,
+                           int32_t *status, void *workspace, uint64_t ws_bytes, void *stream) {
+    Geom g;
+    int32_t r = make_geom(lay, g);
+    if (r != SKV_OK) return r;
+    if ((r = common_checks(g, sigma, counts, status, workspace, ws_bytes, WS_DECODE_MIN)) != SKV_OK)
+        return r;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return SKV_ERR_CUDA;
+    Workspace ws;
+    return decode_tables(g, sigma, counts, status, workspace, ws_bytes, st, ws);
+}
+
+int32_t skv_decode_chunks_prepared(const skv_layout *lay, const void *bitstream,
+                                   uint64_t bitstream_bytes, const uint64_t *offsets, const void *mu,
+                                   const uint32_t *chunk_ids, uint32_t n_ids, void *pages_out,
+                                   int32_t *status, const void *workspace, uint64_t ws_bytes,
+                                   void *stream) {
+    Geom g;
+    int32_t r = make_geom(lay, g);
+    if (r != SKV_OK) return r;
+    if (!status || !workspace || ((uintptr_t)workspace & 255u) != 0) return SKV_ERR_INVALID_ARG;
+    if (ws_bytes < carve(g, WS_DECODE_MIN, nullptr).bytes) return SKV_ERR_INVALID_ARG;
+    if ((r = decode_args_check(g, bitstream, offsets, mu, chunk_ids, n_ids, true, pages_out)) != SKV_OK)
+        return r;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return SKV_ERR_CUDA;
+    const int kind = ws_bytes >= carve(g, WS_DECODE_FULL, nullptr).bytes ? WS_DECODE_FULL : WS_DECODE_MIN;
+    const Workspace ws = carve(g, kind, static_cast<uint8_t *>(const_cast<void *>(workspace)));
+    return decode_launch(g, bitstream, bitstream_bytes, offsets, mu, chunk_ids, n_ids, true, pages_out,
+                         status, ws, st);
 }
 
 int32_t skv_cdf_eval(const skv_layout *lay, const uint64_t *counts, uint64_t n,

@@ -204,6 +204,29 @@ def test_decode_chunks_pages():
         assert np.array_equal(got[i, :n], ref)
 
 
+@pytest.mark.parametrize("W", [64, 256])
+def test_prepared_page_decode(W):
+    cfg = synth.CONFIGS["paged_14b"].scaled(n_layers=2, n_tokens=777, calib_tokens=512)
+    wd, _ = _workload(cfg)
+    lay = H.layout_of(cfg, streams_per_chunk=W)
+    c = Coder(lay)
+    s, offs = c.encode(wd["kv"], wd["mu"], wd["sigma"], wd["counts"])
+    c.prepare_decode(wd["sigma"], wd["counts"])
+    kv = wd["kv"].reshape(lay.n_layers * 2, -1)
+    P = -(-lay.n_tokens // lay.tokens_per_chunk)
+    rng = np.random.default_rng(W)
+    for _ in range(3):
+        ids = torch.tensor(rng.integers(0, lay.n_chunks, 5), dtype=torch.int32, device="cuda")
+        pages = torch.zeros((5, lay.page_elems), dtype=wd["kv"].dtype, device="cuda")
+        c.decode_chunks_prepared_into(s, offs, wd["mu"], ids, pages)
+        c.check_status("prepared")
+        for i, k in enumerate(ids.tolist()):
+            plane, page = divmod(k, P)
+            t0 = page * lay.tokens_per_chunk
+            n = (min(lay.n_tokens, t0 + lay.tokens_per_chunk) - t0) * 1024
+            assert torch.equal(pages[i, :n], kv[plane, t0 * 1024: t0 * 1024 + n])
+
+
 def test_decode_chunks_rejects_bad_id():
     cfg = synth.CONFIGS["tiny"]
     wd, _ = _workload(cfg)
