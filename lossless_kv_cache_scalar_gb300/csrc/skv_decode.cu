@@ -22,6 +22,7 @@
 // of o) is read from per-call inverse tables instead. When the test fails,
 // the whole warp searches for that lane's code together (cooperative_search).
 // Search aids change speed only; the decoded codes are fixed by the exact test.
+#include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
@@ -141,9 +142,8 @@ __device__ __forceinline__ const float2 *dqt() {
 // Round a value to the nearest code (ties to even), clamped to the finite codes.
 template <uint32_t DT> __device__ __forceinline__ uint32_t nearest_ord(float x);
 template <> __device__ __forceinline__ uint32_t nearest_ord<SKV_BF16>(float x) {
-    const uint32_t b = __float_as_uint(x);
-    const uint32_t code = (b + 0x7FFFu + ((b >> 16) & 1u)) >> 16;
-    const uint32_t o = Codes<SKV_BF16>::ord(code & 0xFFFFu);
+    const uint32_t code = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x));
+    const uint32_t o = Codes<SKV_BF16>::ord(code);
     return min(max(o, 0x0080u), 0xFF7Fu);
 }
 template <> __device__ __forceinline__ uint32_t nearest_ord<SKV_E4M3>(float x) {
