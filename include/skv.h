@@ -231,7 +231,7 @@ int32_t skv_cdf_eval(const skv_layout *lay, const uint64_t *counts, uint64_t n,
  * Layouts whose minimum decode scratch (skv_workspace_bytes(lay, 0, ...): the
  * P_hat and quantile tables plus 4 bytes per (layer, kv, channel)) exceeds it
  * are rejected with SKV_ERR_INVALID_ARG before anything is enqueued; 1 MiB
- * covers a bf16 cache of up to 191,360 (layer, kv, channel) sigmas, e.g. 80
+ * covers a bf16 cache of up to 193,920 (layer, kv, channel) sigmas, e.g. 80
  * planes (40 layers, K and V) of 2,048 channels. The outlier inverse tables do
  * not fit, so far outliers are found by bisection (same output, slower).
  *

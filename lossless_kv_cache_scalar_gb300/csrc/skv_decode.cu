@@ -31,9 +31,9 @@
 namespace skv {
 
 constexpr int kDecWarps = 8;
-constexpr uint32_t kRing = 512;        // words per warp ring
-constexpr uint32_t kBlock = 128;       // words per cp.async batch (16 B per lane)
-constexpr uint32_t kStepSyms = 8;      // the ring is topped up every 8 symbols
+constexpr uint32_t kRing = 256;        // words per warp ring
+constexpr uint32_t kBlock = 64;        // words per cp.async batch (16 B per lane, 16 lanes)
+constexpr uint32_t kStepSyms = 4;      // the ring is topped up every 4 symbols
 
 // dynamic shared memory layout (bytes)
 constexpr uint32_t kSmPhi = 0;                                        // Tables
@@ -58,7 +58,7 @@ __device__ float gauss_quantile(float g, float wn, float ww) {
     return 0.5f * (lo + hi);
 }
 
-// qt[i] = (z_i, z_{i+1} - z_i), z_i = G^-1(2^-(1 + i/64)), i = 0..kQuantN.
+// qt[i] = (z_i, z_{i+1} - z_i), z_i = G^-1(2^-(1 + i/32)), i = 0..kQuantN.
 __global__ void __launch_bounds__(256) quant_kernel(const QuantArgs a) {
     const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i > kQuantN) return;
@@ -271,7 +271,7 @@ __device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_g
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 template <uint32_t DT>
-__global__ void __launch_bounds__(kDecWarps * 32, 3) decode_kernel(const DecArgs a) {
+__global__ void __launch_bounds__(kDecWarps * 32, 4) decode_kernel(const DecArgs a) {
     using K = Codes<DT>;
     constexpr uint32_t V = K::V, m = K::m;
     constexpr uint32_t M = 1u << m;
@@ -366,13 +366,13 @@ __global__ void __launch_bounds__(kDecWarps * 32, 3) decode_kernel(const DecArgs
 #pragma unroll 1
         for (uint32_t e = 0; e < V; ++e) {
             if ((e & (kStepSyms - 1u)) == 0u) {
-                // Keep the ring ahead of the reader: 8 symbols use at most 256 words.
+                // Keep the ring ahead of the reader: 4 symbols use at most 128 words.
                 const uint32_t need = min(nw, rp + 32u * kStepSyms);
                 const uint32_t target = min(nwp4, rp + 32u * kStepSyms + kBlock);
                 bool issued_extra = false;
                 while (filled < target) {
                     const uint32_t w0 = filled + 4u * lane;
-                    if (w0 < nwp4) cp_async16(ring + (w0 & (kRing - 1)), words + w0);
+                    if (lane < kBlock / 4 && w0 < nwp4) cp_async16(ring + (w0 & (kRing - 1)), words + w0);
                     cp_async_commit();
                     issued_extra = filled >= need;
                     filled += kBlock;

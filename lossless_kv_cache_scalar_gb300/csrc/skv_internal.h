@@ -111,9 +111,9 @@ struct CompactArgs {
 
 // Decoder search aids (speed only; the output does not depend on them).
 // Quantile table of the Gaussian part G of the mixture in the tail variable
-// t = -log2(g): entry i holds (z_i, z_{i+1} - z_i) with z_i = G^-1(2^-(1 + i/64)),
+// t = -log2(g): entry i holds (z_i, z_{i+1} - z_i) with z_i = G^-1(2^-(1 + i/32)),
 // i = 0..kQuantN; t spans [1, 41], i.e. g down to 2^-41.
-constexpr uint32_t kQuantSteps = 64;
+constexpr uint32_t kQuantSteps = 32;
 constexpr uint32_t kQuantN = 40 * kQuantSteps;
 constexpr uint32_t kQuantFloats = 2 * (kQuantN + 1);
 
