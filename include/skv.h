@@ -218,6 +218,46 @@ int32_t skv_cdf_eval(const skv_layout *lay, const uint64_t *counts, uint64_t n,
                      void *stream);
 
 /*
+ * Histogram of codes: the counts behind p_hat, the empirical marginal of the
+ * wiki's mixture section. counts[b] += the number of i < n with codes[i] == b
+ * (bit pattern; every pattern is counted, NaN codes included), over N = 65536
+ * (bf16) or 256 (e4m3) bins.
+ *  dtype       SKV_BF16 or SKV_E4M3
+ *  codes       device, n codes (uint16 / uint8), aligned to the code size; any
+ *              flat view of a cache (a whole cache, one layer, one page)
+ *  counts      device uint64[N], 8-byte aligned; zeroed first unless accumulate != 0,
+ *              so per-layer or per-rank histograms can be summed in place
+ * No device errors (status is not used). The bf16 kernel runs pairs of CTAs as
+ * a thread-block cluster that share their 32,768 + 32,768 shared-memory bins.
+ */
+int32_t skv_histogram(uint32_t dtype, const void *codes, uint64_t n, uint64_t *counts,
+                      int32_t accumulate, void *stream);
+
+/*
+ * Calibrate sigma once from the first t_cal tokens and freeze it: the
+ * per-(kv, head, channel) scale of the wiki's predictor-choice section and of
+ * the blog's predictor-engineering section, taken per layer as well. The
+ * blog's information-theory section gives the optimum Gaussian scale as the
+ * residual's mean square about mu, so for each (layer, kv, channel):
+ *     r  = fl64(value(kv) - value(mu))   over tokens t < t_cal in ascending order,
+ *                                         elements with both codes finite and
+ *                                         (if mask != NULL) a nonzero mask byte
+ *     S  = sum of fl64(r * r) in binary64, added in that order
+ *     sigma = fl32(sqrt(fl64(S / count)))  (IEEE round to nearest at each step)
+ * clamped into [2^-126, FLT_MAX] so that it is always a valid coding sigma
+ * (no counted element gives 2^-126). Values are in code units (for e4m3, the
+ * stored code's value, before any per-tensor scale).
+ *  kv, mu      device codes in canonical layout
+ *  mask        device uint8, canonical layout like kv, or NULL (count every element):
+ *              leaves outliers out of the calibration, as a clean calibration set would
+ *  t_cal       1 <= t_cal <= n_tokens
+ *  sigma       device float32 [n_layers][n_kv][n_heads][head_dim] (output)
+ * No device errors. Bit-exact: the same inputs always give the same sigma.
+ */
+int32_t skv_calibrate_sigma(const skv_layout *lay, const void *kv, const void *mu, const uint8_t *mask,
+                            uint64_t t_cal, float *sigma, void *stream);
+
+/*
  * Decode without any caller-provided scratch (the pages describe no such
  * call; it serves deployment only). Same contract and outputs as skv_decode,
  * minus the workspace arguments. It is meant for callers that cannot call

@@ -45,6 +45,8 @@ SIGNATURES = {
     "skv_decode_noalloc": (_i32, [_LP, _vp, _u64, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "skv_decode_prepare": (_i32, [_LP, _vp, _vp, _vp, _vp, _u64, _vp]),
     "skv_decode_chunks_prepared": (_i32, [_LP, _vp, _u64, _vp, _vp, _vp, _u32, _vp, _vp, _vp, _u64, _vp]),
+    "skv_histogram": (_i32, [_u32, _vp, _u64, _vp, _i32, _vp]),
+    "skv_calibrate_sigma": (_i32, [_LP, _vp, _vp, _vp, _u64, _vp, _vp]),
 }
 
 _lib = None

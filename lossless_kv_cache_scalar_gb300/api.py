@@ -239,3 +239,50 @@ def decode(layout: Layout, bitstream, offsets, mu, sigma, counts, stream=None):
 def decode_chunks(layout: Layout, bitstream, offsets, mu, sigma, counts, chunk_ids, stream=None):
     return Coder(layout, mu.device, encode=False).decode_chunks(bitstream, offsets, mu, sigma,
                                                                 counts, chunk_ids, stream)
+
+
+def histogram(codes: torch.Tensor, dtype: str | None = None, counts: torch.Tensor | None = None,
+              stream=None) -> torch.Tensor:
+    """Code histogram (skv_histogram): int64 [N] counts of every bit pattern.
+
+    `codes` is any contiguous CUDA tensor of 2-byte (bf16) or 1-byte (e4m3)
+    codes; with `counts` given, the histogram is added to it in place.
+    """
+    if not codes.is_cuda or not codes.is_contiguous():
+        raise ValueError("codes must be a contiguous CUDA tensor")
+    if dtype is None:
+        dtype = "bf16" if codes.element_size() == 2 else "e4m3"
+    n_codes = 65536 if dtype == "bf16" else 256
+    if codes.element_size() != (2 if dtype == "bf16" else 1):
+        raise ValueError(f"{dtype} codes must be {2 if dtype == 'bf16' else 1}-byte elements")
+    acc = counts is not None
+    if acc:
+        if counts.dtype != torch.int64 or counts.numel() != n_codes or not counts.is_cuda:
+            raise ValueError(f"counts must be an int64 CUDA tensor of {n_codes} entries")
+    else:
+        counts = torch.empty(n_codes, dtype=torch.int64, device=codes.device)
+    rc = B.lib().skv_histogram(_DT[dtype], _ptr(codes), codes.numel(), _ptr(counts), int(acc),
+                               _stream_handle(stream))
+    B.check("skv_histogram", rc)
+    return counts
+
+
+def calibrate_sigma(layout: Layout, kv: torch.Tensor, mu: torch.Tensor, t_cal: int,
+                    mask: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Frozen per-(layer, kv, head, channel) sigma from tokens < t_cal (skv_calibrate_sigma).
+
+    `mask` (bool or uint8, the layout of kv) keeps only the elements it marks.
+    Returns float32 [n_layers][n_kv][n_heads][head_dim].
+    """
+    _check_codes(kv, layout, "kv")
+    _check_codes(mu, layout, "mu")
+    if mask is not None:
+        if not mask.is_cuda or not mask.is_contiguous() or mask.element_size() != 1 \
+                or mask.numel() != layout.n_elems:
+            raise ValueError("mask must be a contiguous 1-byte CUDA tensor shaped like kv")
+    sigma = torch.empty((layout.n_layers, layout.n_kv, layout.n_heads, layout.head_dim),
+                        dtype=torch.float32, device=kv.device)
+    rc = B.lib().skv_calibrate_sigma(C.byref(layout.c()), _ptr(kv), _ptr(mu), _ptr(mask), int(t_cal),
+                                     _ptr(sigma), _stream_handle(stream))
+    B.check("skv_calibrate_sigma", rc)
+    return sigma

@@ -13,6 +13,10 @@ int launch_encode(const EncArgs &a, cudaStream_t st);
 int launch_scan(const ScanArgs &a, cudaStream_t st);
 int launch_compact(const CompactArgs &a, cudaStream_t st);
 int launch_decode(const DecArgs &a, cudaStream_t st);
+int launch_histogram(uint32_t dtype, const void *codes, uint64_t n, unsigned long long *counts,
+                     cudaStream_t st);
+int launch_calibrate(const Geom &g, const void *kv, const void *mu, const uint8_t *mask,
+                     uint64_t t_cal, float *sigma, cudaStream_t st);
 int launch_search_aids(const Geom &g, const uint32_t *phat, float *qt, uint16_t *inv_lo,
                        uint16_t *inv_hi, cudaStream_t st);
 
@@ -499,6 +503,32 @@ int32_t skv_cdf_eval(const skv_layout *lay, const uint64_t *counts, uint64_t n,
     if (g.dtype == SKV_BF16) cdf_eval_kernel<SKV_BF16><<<(unsigned)blocks, 256, 0, st>>>(ca);
     else cdf_eval_kernel<SKV_E4M3><<<(unsigned)blocks, 256, 0, st>>>(ca);
     return cudaGetLastError() == cudaSuccess ? SKV_OK : SKV_ERR_CUDA;
+}
+
+int32_t skv_histogram(uint32_t dtype, const void *codes, uint64_t n, uint64_t *counts,
+                      int32_t accumulate, void *stream) {
+    if (dtype != SKV_BF16 && dtype != SKV_E4M3) return SKV_ERR_INVALID_ARG;
+    const DtypeInfo d = dtype_info(dtype);
+    if (!counts || ((uintptr_t)counts & 7u) != 0) return SKV_ERR_INVALID_ARG;
+    if (n && (!codes || ((uintptr_t)codes % d.bytes) != 0)) return SKV_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!accumulate && cudaMemsetAsync(counts, 0, sizeof(uint64_t) * d.N, st) != cudaSuccess)
+        return SKV_ERR_CUDA;
+    return launch_histogram(dtype, codes, n, reinterpret_cast<unsigned long long *>(counts), st)
+               ? SKV_ERR_CUDA : SKV_OK;
+}
+
+int32_t skv_calibrate_sigma(const skv_layout *lay, const void *kv, const void *mu, const uint8_t *mask,
+                            uint64_t t_cal, float *sigma, void *stream) {
+    Geom g;
+    int32_t r = make_geom(lay, g);
+    if (r != SKV_OK) return r;
+    if (t_cal == 0 || t_cal > g.T || !kv || !mu || !sigma) return SKV_ERR_INVALID_ARG;
+    const uint32_t b = dtype_info(g.dtype).bytes;
+    if (((uintptr_t)kv % b) != 0 || ((uintptr_t)mu % b) != 0 || ((uintptr_t)sigma & 3u) != 0)
+        return SKV_ERR_INVALID_ARG;
+    return launch_calibrate(g, kv, mu, mask, t_cal, sigma, static_cast<cudaStream_t>(stream))
+               ? SKV_ERR_CUDA : SKV_OK;
 }
 
 }  // extern "C"

@@ -104,6 +104,8 @@ def lib():
         L.oracle_ideal_bits.argtypes = [C.POINTER(_Layout), vp, vp, vp, vp]
         L.oracle_model_bits.restype = C.c_double
         L.oracle_model_bits.argtypes = [C.POINTER(_Layout), vp, vp, vp, vp]
+        L.oracle_histogram.argtypes = [u32, vp, u64, vp, C.c_int]
+        L.oracle_calibrate_sigma.argtypes = [C.POINTER(_Layout), vp, vp, vp, u64, vp]
         _lib = L
     return _lib
 
@@ -261,3 +263,29 @@ def ideal_bits(lay: Layout, kv, mu, sigma, counts) -> float:
 def model_bits(lay: Layout, kv, mu, sigma, counts) -> float:
     kv, mu, sigma, counts = _inputs(lay, kv, mu, sigma, counts)
     return lib().oracle_model_bits(C.byref(lay.c()), _p(kv), _p(mu), _p(sigma), _p(counts))
+
+
+# ------------------------------------------------- model inputs: p_hat, sigma
+
+def histogram(dtype: int, codes, counts=None) -> np.ndarray:
+    """Counts of every code bit pattern (uint64[N]); adds to `counts` if given."""
+    n = 65536 if dtype == BF16 else 256
+    codes = np.ascontiguousarray(codes, np.uint16 if dtype == BF16 else np.uint8).reshape(-1)
+    acc = counts is not None
+    out = np.ascontiguousarray(counts, np.uint64).copy() if acc else np.zeros(n, np.uint64)
+    _check(lib().oracle_histogram(dtype, _p(codes), codes.size, _p(out), int(acc)))
+    return out
+
+
+def calibrate_sigma(lay: Layout, kv: np.ndarray, mu: np.ndarray, t_cal: int,
+                    mask: np.ndarray | None = None) -> np.ndarray:
+    """Frozen per-channel sigma (float32 [n_layers][n_kv][H][D]) from tokens < t_cal."""
+    cd = lay.code_dtype
+    kv = np.ascontiguousarray(kv).view(cd)
+    mu = np.ascontiguousarray(mu).view(cd)
+    if mask is not None:
+        mask = np.ascontiguousarray(mask).view(np.uint8)
+    out = np.zeros((lay.n_layers, lay.n_kv, lay.n_heads, lay.head_dim), np.float32)
+    _check(lib().oracle_calibrate_sigma(C.byref(lay.c()), _p(kv), _p(mu), _p(mask), int(t_cal),
+                                        _p(out)))
+    return out

@@ -850,3 +850,67 @@ double oracle_model_bits(const or_layout *lay, const void *kv, const void *mu,
     setup_free(&su);
     return bits;
 }
+
+/* ------------------------------------- inputs of the model: p_hat and sigma */
+
+/*
+ * counts[b] = number of codes equal to b (every bit pattern, NaN codes too):
+ * the empirical marginal p_hat of the wiki's mixture section, before
+ * normalisation. Adds to counts when accumulate is nonzero, else starts from 0.
+ */
+int oracle_histogram(uint32_t dtype, const void *codes, uint64_t n, uint64_t *counts,
+                     int accumulate)
+{
+    if (dtype > DT_E4M3 || !counts || (n && !codes)) return OR_ERR_INVALID_ARG;
+    uint32_t N = dtype_info(dtype).N;
+    if (!accumulate) memset(counts, 0, sizeof(uint64_t) * N);
+    for (uint64_t i = 0; i < n; ++i) {
+        uint32_t b = dtype == DT_BF16 ? ((const uint16_t *)codes)[i] : ((const uint8_t *)codes)[i];
+        counts[b] += 1;
+    }
+    return OR_OK;
+}
+
+/*
+ * Frozen per-(layer, kv, head, channel) sigma from the first t_cal tokens:
+ * the calibrate-once scale of the wiki's predictor-choice section and the
+ * blog's predictor-engineering section. The blog's information-theory section
+ * gives the Gaussian code length's optimum as the mean squared residual about
+ * mu, so sigma is the root mean square of r = value(kv) - value(mu) over the
+ * counted elements (both codes finite; mask byte nonzero when a mask is
+ * given), summed in binary64 in token order and rounded to binary32 at the
+ * end, then clamped into the valid range [2^-126, FLT_MAX] (2^-126 when
+ * nothing is counted).
+ */
+int oracle_calibrate_sigma(const or_layout *lay, const void *kv, const void *mu,
+                           const uint8_t *mask, uint64_t t_cal, float *sigma)
+{
+    or_geom g;
+    int st = geom_init(lay, &g);
+    if (st != OR_OK) return st;
+    if (t_cal == 0 || t_cal > lay->n_tokens || !kv || !mu || !sigma) return OR_ERR_INVALID_ARG;
+    uint64_t planes = (uint64_t)lay->n_layers * lay->n_kv;
+    for (uint64_t p = 0; p < planes; ++p) {
+        for (uint64_t c = 0; c < g.HD; ++c) {
+            double S = 0.0;
+            uint64_t count = 0;
+            for (uint64_t t = 0; t < t_cal; ++t) {
+                uint64_t el = (p * lay->n_tokens + t) * g.HD + c;
+                if (mask && mask[el] == 0) continue;
+                uint32_t kb = load_code(&g, kv, el), mb = load_code(&g, mu, el);
+                if (!code_is_finite(lay->dtype, kb) || !code_is_finite(lay->dtype, mb)) continue;
+                double r = (double)oracle_value(lay->dtype, kb) - (double)oracle_value(lay->dtype, mb);
+                S += r * r;
+                count += 1;
+            }
+            float s = 0x1p-126f;
+            if (count) {
+                s = (float)sqrt(S / (double)count);
+                if (!(s >= 0x1p-126f)) s = 0x1p-126f;
+                if (s > 0x1.fffffep127f) s = 0x1.fffffep127f;
+            }
+            sigma[p * g.HD + c] = s;
+        }
+    }
+    return OR_OK;
+}
