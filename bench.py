@@ -169,6 +169,8 @@ def main():
     ap.add_argument("--tokens", type=int, default=None, help="override n_tokens (profiling cases)")
     ap.add_argument("--page-latency", type=int, default=200,
                     help="single-page random decodes timed after the run (0: skip)")
+    ap.add_argument("--model-inputs", type=int, default=1,
+                    help="time skv_histogram and skv_calibrate_sigma on the workload (0: skip)")
     ap.add_argument("--traffic-json", default=os.path.join(ROOT, "profiles", "traffic.json"))
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "skv" else args.warmup
@@ -255,6 +257,7 @@ def main():
         traffic = None
     hbm_peak = _peaks().get("hbm_gbs", 6685.5)
     page_lat = page_latency(coder, out, offsets, w, lay, args, dev) if args.page_latency else None
+    inputs = model_inputs_run(w, lay, args, dev, hbm_peak) if args.model_inputs else None
     bits = 8.0 * total_bytes / n_el
 
     # end to end through the public API with host buffers
@@ -295,6 +298,7 @@ def main():
             "roofline_decode_frac": ALG_OPS[(lay.dtype, "decode")] * n_el / (t_dec / args.steps) / 1e12 / peak_tops,
             "cpu_baseline": cpu,
             "page_decode_latency_us": page_lat,
+            "model_inputs": inputs,
             "e2e": e2e,
             "gpu_launches": 8 * args.steps,
             "clocks": clocks,
@@ -331,6 +335,51 @@ def page_latency(coder, out, offsets, w, lay, args, dev):
             "pages": int(len(ids)), "page_scalars": lay.page_elems,
             "streams_per_chunk": lay.streams_per_chunk,
             "note": "one 256-token page per skv_decode_chunks_prepared call, tables prepared once"}
+
+
+def model_inputs_run(w, lay, args, dev, hbm_peak, reps=5):
+    """The two steps before the coder, on the bench workload: the code
+    histogram over every scalar (checked against the workload's counts) and
+    the sigma calibration over the first 1,024 tokens. Median device time of
+    `reps` calls (CUDA events on the launching stream, 3 untimed calls first);
+    the inputs (>> L2) are not reused between calls of the histogram."""
+    import lossless_kv_cache_scalar_gb300 as skv
+    stream = torch.cuda.Stream(device=dev)
+    t_cal = min(1024, lay.n_tokens)
+    counts = torch.empty_like(w["counts"])
+
+    def timed(fn):
+        ts = []
+        with torch.cuda.stream(stream):
+            for i in range(3 + reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                stream.synchronize()
+                if i >= 3:
+                    ts.append(e0.elapsed_time(e1))
+        return float(np.median(ts))
+
+    def hist():
+        counts.zero_()
+        skv.histogram(w["kv"], lay.dtype, counts=counts, stream=stream)
+
+    t_h = timed(hist)
+    if not torch.equal(counts, w["counts"]):
+        raise SystemExit("bench: skv_histogram differs from the workload's counts")
+    t_c = timed(lambda: skv.calibrate_sigma(lay, w["kv"], w["mu"], t_cal, stream=stream))
+    hist_bytes = lay.n_elems * lay.bytes_per_code
+    cal_elems = lay.n_layers * lay.n_kv * t_cal * lay.n_heads * lay.head_dim
+    cal_bytes = cal_elems * 2 * lay.bytes_per_code
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    return {"histogram_ms": t_h, "histogram_gbs": hist_bytes / t_h / 1e6,
+            "histogram_hbm_frac": hist_bytes / t_h / 1e6 / hbm_peak,
+            "calibrate_ms": t_c, "calibrate_tokens": t_cal, "calibrate_gbs": cal_bytes / t_c / 1e6,
+            "calibrate_f64_gops": 3 * cal_elems / t_c / 1e6,
+            "calibrate_bound": "fp64 pipe (3 binary64 ops per element; %d SMs)" % sms,
+            "note": "histogram over all scalars (counts checked equal to the workload's); "
+                    "sigma from tokens < %d without a mask; median of %d calls" % (t_cal, reps)}
 
 
 def e2e_run(coder, w, lay, args, dev, total_bytes):

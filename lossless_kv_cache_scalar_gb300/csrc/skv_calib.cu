@@ -15,42 +15,35 @@ namespace skv {
 
 // ---------------------------------------------------------------- histogram
 
-// bf16: 65,536 u32 bins (256 KB) do not fit one CTA's shared memory, so the
-// bins are split by the code's top bit between the two CTAs of a cluster,
-// 32,768 bins (128 KB) each. Both CTAs of a pair read the same tiles of codes
-// at the same time (the second read of a line is an L2 hit, so HBM sees each
-// byte about once) and each counts the codes of its own half with plain
-// shared-memory atomics. The cluster launch only guarantees that the pair runs
-// together; no shared memory is exchanged (remote red.shared::cluster adds
-// measured several times slower than reading the codes twice). At the end each
-// CTA adds its nonzero bins to the u64 counts.
+// bf16: all 65,536 u32 bins (256 KB) do not fit one CTA's shared memory, but
+// the codes whose biased exponent is below 192 (|value| < 2^65, both signs:
+// 2 x 24,576 codes, 192 KB) do, and a KV cache holds almost nothing else. So
+// each CTA (one per SM) counts those in shared memory and adds the rest (if
+// any) straight to the u64 counts in global memory; at the end it adds its
+// nonzero shared bins to the counts. The result is exact for any input; only
+// the speed depends on the values.
 constexpr int kHistThreads = 1024;
-constexpr int kHistUnroll = 4;        // 16-byte loads in flight per thread
+constexpr int kHistUnroll = 4;             // 16-byte loads in flight per thread
+constexpr uint32_t kHistHalf = 192u << 7;  // codes per sign kept in shared memory
+constexpr int kHistSmem = 2 * kHistHalf * sizeof(uint32_t);
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHistThreads, 1)
+__global__ void __launch_bounds__(kHistThreads, 1)
     hist_bf16_kernel(const uint16_t *__restrict__ codes, uint64_t n, uint32_t head,
                      unsigned long long *__restrict__ counts) {
-    extern __shared__ uint32_t bins[];                    // the 32,768 bins of this CTA's half
-    const uint32_t rank = cluster_ctarank();
-    for (uint32_t i = threadIdx.x; i < 32768u; i += blockDim.x) bins[i] = 0u;
+    extern __shared__ uint32_t bins[];     // [sign][code & 0x7FFF < kHistHalf]
+    for (uint32_t i = threadIdx.x; i < 2 * kHistHalf; i += blockDim.x) bins[i] = 0u;
     __syncthreads();
-    const uint32_t mine = rank << 15;
     auto add = [&](uint32_t code) {
-        if ((code & 0x8000u) == mine) atomicAdd(&bins[code & 0x7FFFu], 1u);
+        const uint32_t mag = code & 0x7FFFu;
+        if (mag < kHistHalf) atomicAdd(&bins[(code >> 15) * kHistHalf + mag], 1u);
+        else atomicAdd(counts + code, 1ull);
     };
     auto add2 = [&](uint32_t w) { add(w & 0xFFFFu); add(w >> 16); };
     // codes[head .. head + 8 nvec) are 16-byte aligned; the rest go one by one
     const uint64_t nvec = (n - head) / 8;
     const uint4 *vec = reinterpret_cast<const uint4 *>(codes + head);
-    const uint64_t pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
-    const uint64_t stride = n_pairs * blockDim.x;
-    uint64_t v = pair * blockDim.x + threadIdx.x;
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    uint64_t v = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
     for (; v + (kHistUnroll - 1) * stride < nvec; v += kHistUnroll * stride) {
         uint4 q[kHistUnroll];
 #pragma unroll
@@ -62,15 +55,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHistThreads, 1)
         const uint4 q = __ldg(vec + v);
         add2(q.x); add2(q.y); add2(q.z); add2(q.w);
     }
-    if (pair == 0) {
+    if (blockIdx.x == 0) {
         const uint64_t tail0 = head + 8 * nvec;
         if (threadIdx.x < head) add(codes[threadIdx.x]);
         if (threadIdx.x < n - tail0) add(codes[tail0 + threadIdx.x]);
     }
     __syncthreads();
-    for (uint32_t i = threadIdx.x; i < 32768u; i += blockDim.x) {
+    for (uint32_t i = threadIdx.x; i < 2 * kHistHalf; i += blockDim.x) {
         const uint32_t c = bins[i];
-        if (c) atomicAdd(counts + mine + i, (unsigned long long)c);
+        const uint32_t code = (i >= kHistHalf ? 0x8000u : 0u) | (i % kHistHalf);
+        if (c) atomicAdd(counts + code, (unsigned long long)c);
     }
 }
 
@@ -222,13 +216,11 @@ int launch_histogram(uint32_t dtype, const void *codes, uint64_t n, unsigned lon
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return 1;
     if (dtype == SKV_BF16) {
-        const int smem = 32768 * (int)sizeof(uint32_t);
-        if (cudaFuncSetAttribute(hist_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        if (cudaFuncSetAttribute(hist_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kHistSmem) !=
             cudaSuccess)
             return 1;
-        const unsigned grid = sms >= 2 ? (unsigned)(sms & ~1) : 2u;   // one CTA per SM, whole pairs
-        hist_bf16_kernel<<<grid, kHistThreads, smem, st>>>(static_cast<const uint16_t *>(codes), n,
-                                                           (uint32_t)head, counts);
+        hist_bf16_kernel<<<(unsigned)sms, kHistThreads, kHistSmem, st>>>(static_cast<const uint16_t *>(codes),
+                                                                          n, (uint32_t)head, counts);
     } else {
         hist_e4m3_kernel<<<(unsigned)(sms * 4), kHist8Warps * 32, 0, st>>>(
             static_cast<const uint8_t *>(codes), n, (uint32_t)head, counts);
