@@ -169,6 +169,9 @@ def main():
     ap.add_argument("--tokens", type=int, default=None, help="override n_tokens (profiling cases)")
     ap.add_argument("--page-latency", type=int, default=200,
                     help="single-page random decodes timed after the run (0: skip)")
+    ap.add_argument("--sigma-block", type=int, default=0,
+                    help="tokens per sigma block (0: the workload's frozen per-channel sigma); "
+                         "blocks are calibrated on the device from their own tokens")
     ap.add_argument("--model-inputs", type=int, default=1,
                     help="time skv_histogram and skv_calibrate_sigma on the workload (0: skip)")
     ap.add_argument("--traffic-json", default=os.path.join(ROOT, "profiles", "traffic.json"))
@@ -190,9 +193,16 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     cfg = cfg.scaled(seed=cfg.seed + 1000 * rank) if world > 1 else cfg
-    w = synth.generate(cfg, device=dev)
+    w = synth.generate(cfg, device=dev, with_mask=args.sigma_block > 0)
     lay = skv.Layout(cfg.dtype, cfg.n_layers, cfg.n_kv, cfg.n_heads, cfg.head_dim, cfg.n_tokens,
-                     streams_per_chunk=args.streams)
+                     streams_per_chunk=args.streams, sigma_block_tokens=args.sigma_block)
+    if args.sigma_block:
+        # position-aware sigma: each block's own RMS over its Gaussian-drawn elements
+        mask = w.pop("mask").view(torch.uint8)
+        w["sigma"] = skv.calibrate_sigma(lay, w["kv"], w["mu"], min(args.sigma_block, cfg.n_tokens),
+                                         mask=mask)
+        del mask
+    sigma_side_bits = 32.0 * w["sigma"].numel() / lay.n_elems
     coder = skv.Coder(lay, dev)
     out, offsets = coder.alloc_output()
     back = torch.empty_like(w["mu"])
@@ -285,9 +295,11 @@ def main():
                                                        cfg.head_dim],
                        "code_dtype": cfg.dtype, "scalars": n_el, "tokens_per_chunk": lay.tokens_per_chunk,
                        "streams_per_chunk": lay.streams_per_chunk, "weights": list(lay.weights),
+                       "sigma_block_tokens": lay.sigma_block_tokens,
                        "l2": "inputs 2 x %.1f GB >> 129 MB L2, no flush" % (raw_bytes / 1e9)},
             "encode_gbs": enc_gbs, "decode_gbs": dec_gbs, "bits_per_scalar": bits,
             "compression_ratio": 8.0 * lay.bytes_per_code / bits,
+            "sigma_side_bits_per_scalar": sigma_side_bits,
             "roofline": {"bound": "alu", "kernel": dom, "achieved": achieved, "peak": peak_tops,
                          "unit": "Tops/s", "frac": achieved / peak_tops, "traffic": traffic,
                          "alg_ops_per_scalar": ALG_OPS[(lay.dtype, dom)],
@@ -345,7 +357,7 @@ def model_inputs_run(w, lay, args, dev, hbm_peak, reps=5):
     the inputs (>> L2) are not reused between calls of the histogram."""
     import lossless_kv_cache_scalar_gb300 as skv
     stream = torch.cuda.Stream(device=dev)
-    t_cal = min(1024, lay.n_tokens)
+    t_cal = min(1024, lay.n_tokens, lay.sigma_block_tokens or lay.n_tokens)
     counts = torch.empty_like(w["counts"])
 
     def timed(fn):

@@ -29,7 +29,8 @@
  *    the first error found wins. The device never traps.
  *  - Tensor layout is canonical: KV and mu are [n_layers][n_kv][n_tokens]
  *    [n_heads][head_dim] codes, channel fastest, 16-byte aligned; sigma is
- *    float32 [n_layers][n_kv][n_heads][head_dim]; counts is uint64[N], N =
+ *    float32 [n_layers][n_kv][n_heads][head_dim] (with sigma blocks,
+ *    [n_layers][n_kv][n_blocks][n_heads][head_dim]); counts is uint64[N], N =
  *    65536 (bf16) or 256 (e4m3), indexed by code bit pattern.
  */
 #ifndef SKV_H
@@ -60,7 +61,7 @@ enum {
 };
 
 /*
- * What is coded and how it is cut (FORMAT.md section 7).
+ * What is coded and how it is cut (FORMAT.md sections 4 and 7).
  *  version            SKV_FORMAT_VERSION
  *  dtype              SKV_BF16 or SKV_E4M3
  *  n_layers, n_kv     planes; n_kv is 2 for K and V
@@ -71,6 +72,14 @@ enum {
  *  streams_per_chunk  W = 32 * G, G in 1..8: interleaved rANS streams per chunk
  *  w_narrow, w_wide, w_marginal  integer mixture weights, sum 100 (the wiki's
  *                     0.95 / 0.03 / 0.02 are 95 / 3 / 2)
+ *  sigma_block_tokens B: 0 gives one sigma per (layer, kv, head, channel) for all
+ *                     tokens, the calibrated-once, frozen scale of the wiki's
+ *                     predictor-choice section. B > 0 (a multiple of
+ *                     tokens_per_chunk) gives one sigma per block of B tokens:
+ *                     sigma is then [n_layers][n_kv][ceil(n_tokens / B)][n_heads]
+ *                     [head_dim] and token t uses block t / B; this is the
+ *                     position-aware sigma the blog's limitations section leaves
+ *                     to future work. The bitstream format does not change.
  */
 typedef struct skv_layout {
     uint32_t version;
@@ -85,7 +94,7 @@ typedef struct skv_layout {
     uint32_t w_narrow;
     uint32_t w_wide;
     uint32_t w_marginal;
-    uint32_t reserved;          /* must be 0 */
+    uint32_t sigma_block_tokens; /* 0, or a multiple of tokens_per_chunk (see below) */
 } skv_layout;
 
 /* Library build/format version: returns SKV_FORMAT_VERSION. */
@@ -134,7 +143,8 @@ int32_t skv_workspace_bytes(const skv_layout *lay, int32_t op, uint64_t *bytes);
 /*
  * Encode a whole KV cache (the encoder of the wiki's pipeline section).
  *  kv, mu        device, codes in canonical layout (uint16 bf16 / uint8 e4m3), 16-byte aligned
- *  sigma         device float32 [n_layers][n_kv][n_heads][head_dim]
+ *  sigma         device float32 [n_layers][n_kv][n_heads][head_dim], or per sigma
+ *                block (see skv_layout)
  *  counts        device uint64[N], the marginal histogram (may be NULL iff w_marginal == 0);
  *                its sum must be below 2^63
  *  out           device, out_capacity bytes, 16-byte aligned: receives the chunks back to back
@@ -227,8 +237,9 @@ int32_t skv_cdf_eval(const skv_layout *lay, const uint64_t *counts, uint64_t n,
  *              flat view of a cache (a whole cache, one layer, one page)
  *  counts      device uint64[N], 8-byte aligned; zeroed first unless accumulate != 0,
  *              so per-layer or per-rank histograms can be summed in place
- * No device errors (status is not used). The bf16 kernel runs pairs of CTAs as
- * a thread-block cluster that share their 32,768 + 32,768 shared-memory bins.
+ * No device errors (status is not used). The bf16 kernel keeps the codes of
+ * magnitude below 2^65 in 192 KB of shared-memory bins per SM and adds any
+ * others straight to counts, so it is exact for every input.
  */
 int32_t skv_histogram(uint32_t dtype, const void *codes, uint64_t n, uint64_t *counts,
                       int32_t accumulate, void *stream);
@@ -238,8 +249,10 @@ int32_t skv_histogram(uint32_t dtype, const void *codes, uint64_t n, uint64_t *c
  * per-(kv, head, channel) scale of the wiki's predictor-choice section and of
  * the blog's predictor-engineering section, taken per layer as well. The
  * blog's information-theory section gives the optimum Gaussian scale as the
- * residual's mean square about mu, so for each (layer, kv, channel):
- *     r  = fl64(value(kv) - value(mu))   over tokens t < t_cal in ascending order,
+ * residual's mean square about mu, so for each (layer, kv, channel) -- and,
+ * when lay->sigma_block_tokens = B > 0, for each block of B tokens, from the
+ * first t_cal tokens of that block:
+ *     r  = fl64(value(kv) - value(mu))   over those tokens in ascending order,
  *                                         elements with both codes finite and
  *                                         (if mask != NULL) a nonzero mask byte
  *     S  = sum of fl64(r * r) in binary64, added in that order
@@ -250,8 +263,10 @@ int32_t skv_histogram(uint32_t dtype, const void *codes, uint64_t n, uint64_t *c
  *  kv, mu      device codes in canonical layout
  *  mask        device uint8, canonical layout like kv, or NULL (count every element):
  *              leaves outliers out of the calibration, as a clean calibration set would
- *  t_cal       1 <= t_cal <= n_tokens
- *  sigma       device float32 [n_layers][n_kv][n_heads][head_dim] (output)
+ *  t_cal       1 <= t_cal <= n_tokens, and t_cal <= B with sigma blocks (a shorter
+ *              last block uses all of its tokens)
+ *  sigma       device float32 [n_layers][n_kv][n_heads][head_dim], or
+ *              [n_layers][n_kv][n_blocks][n_heads][head_dim] with sigma blocks (output)
  * No device errors. Bit-exact: the same inputs always give the same sigma.
  */
 int32_t skv_calibrate_sigma(const skv_layout *lay, const void *kv, const void *mu, const uint8_t *mask,

@@ -23,7 +23,8 @@ class skv_layout(C.Structure):
                 ("n_kv", C.c_uint32), ("n_heads", C.c_uint32), ("head_dim", C.c_uint32),
                 ("n_tokens", C.c_uint64), ("tokens_per_chunk", C.c_uint32),
                 ("streams_per_chunk", C.c_uint32), ("w_narrow", C.c_uint32),
-                ("w_wide", C.c_uint32), ("w_marginal", C.c_uint32), ("reserved", C.c_uint32)]
+                ("w_wide", C.c_uint32), ("w_marginal", C.c_uint32),
+                ("sigma_block_tokens", C.c_uint32)]
 
 
 # name -> (restype, argtypes); the exported symbols of include/skv.h

@@ -28,12 +28,24 @@ class Layout:
     tokens_per_chunk: int = 256
     streams_per_chunk: int = 64
     weights: tuple = (95, 3, 2)
+    sigma_block_tokens: int = 0   # 0: one sigma per channel; else tokens per sigma block
 
     def c(self) -> B.skv_layout:
         w = self.weights
         return B.skv_layout(B.SKV_FORMAT_VERSION, _DT[self.dtype], self.n_layers, self.n_kv,
                             self.n_heads, self.head_dim, self.n_tokens, self.tokens_per_chunk,
-                            self.streams_per_chunk, w[0], w[1], w[2], 0)
+                            self.streams_per_chunk, w[0], w[1], w[2], self.sigma_block_tokens)
+
+    @property
+    def n_sigma_blocks(self) -> int:
+        b = self.sigma_block_tokens
+        return -(-self.n_tokens // b) if b else 1
+
+    @property
+    def sigma_shape(self) -> tuple:
+        if self.sigma_block_tokens:
+            return (self.n_layers, self.n_kv, self.n_sigma_blocks, self.n_heads, self.head_dim)
+        return (self.n_layers, self.n_kv, self.n_heads, self.head_dim)
 
     @property
     def n_codes(self) -> int:
@@ -87,6 +99,20 @@ def _stream_handle(stream: torch.cuda.Stream | None):
     return C.c_void_p(s.cuda_stream)
 
 
+def _check_model_inputs(lay: Layout, sigma: torch.Tensor, counts: torch.Tensor | None):
+    """sigma and counts must be device tensors of the layout's sizes (the C ABI
+    takes bare pointers, so a short table would be read past its end)."""
+    n_sig = 1
+    for d in lay.sigma_shape:
+        n_sig *= d
+    if not sigma.is_cuda or not sigma.is_contiguous() or sigma.dtype != torch.float32 \
+            or sigma.numel() != n_sig:
+        raise ValueError(f"sigma must be a contiguous float32 CUDA tensor of shape {lay.sigma_shape}")
+    if counts is not None and (not counts.is_cuda or counts.dtype != torch.int64
+                               or counts.numel() != lay.n_codes or not counts.is_contiguous()):
+        raise ValueError(f"counts must be a contiguous int64 CUDA tensor of {lay.n_codes} entries")
+
+
 def _check_codes(t: torch.Tensor, lay: Layout, what: str):
     if not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{what} must be a contiguous CUDA tensor")
@@ -134,6 +160,7 @@ class Coder:
         lay = self.layout
         _check_codes(kv, lay, "kv")
         _check_codes(mu, lay, "mu")
+        _check_model_inputs(lay, sigma, counts)
         rc = B.lib().skv_encode(C.byref(self._c), _ptr(kv), _ptr(mu), _ptr(sigma), _ptr(counts),
                                 _ptr(out), out.numel(), _ptr(offsets), _ptr(self.status),
                                 _ptr(self.workspace), self.workspace.numel(),
@@ -153,6 +180,7 @@ class Coder:
         lay = self.layout
         _check_codes(mu, lay, "mu")
         _check_codes(kv_out, lay, "kv_out")
+        _check_model_inputs(lay, sigma, counts)
         rc = B.lib().skv_decode(C.byref(self._c), _ptr(bitstream), bitstream.numel(),
                                 _ptr(offsets), _ptr(mu), _ptr(sigma), _ptr(counts), _ptr(kv_out),
                                 _ptr(self.status), _ptr(self.workspace), self.workspace.numel(),
@@ -173,6 +201,8 @@ class Coder:
             raise ValueError("chunk_ids must be an int32 CUDA tensor")
         if pages_out.numel() != ids.numel() * lay.page_elems:
             raise ValueError("pages_out must hold n_ids * tokens_per_chunk * HD codes")
+        _check_codes(mu, lay, "mu")
+        _check_model_inputs(lay, sigma, counts)
         rc = B.lib().skv_decode_chunks(C.byref(self._c), _ptr(bitstream), bitstream.numel(),
                                        _ptr(offsets), _ptr(mu), _ptr(sigma), _ptr(counts), _ptr(ids),
                                        ids.numel(), _ptr(pages_out), _ptr(self.status),
@@ -182,6 +212,7 @@ class Coder:
 
     def prepare_decode(self, sigma, counts, stream=None, check: bool = True):
         """Build the decoder tables once (skv_decode_prepare) for decode_chunks_prepared."""
+        _check_model_inputs(self.layout, sigma, counts)
         rc = B.lib().skv_decode_prepare(C.byref(self._c), _ptr(sigma), _ptr(counts), _ptr(self.status),
                                         _ptr(self.workspace), self.workspace.numel(),
                                         _stream_handle(stream))
@@ -272,7 +303,9 @@ def calibrate_sigma(layout: Layout, kv: torch.Tensor, mu: torch.Tensor, t_cal: i
     """Frozen per-(layer, kv, head, channel) sigma from tokens < t_cal (skv_calibrate_sigma).
 
     `mask` (bool or uint8, the layout of kv) keeps only the elements it marks.
-    Returns float32 [n_layers][n_kv][n_heads][head_dim].
+    Returns float32 [n_layers][n_kv][n_heads][head_dim], or with sigma blocks
+    [n_layers][n_kv][n_blocks][n_heads][head_dim] (each block from its own first
+    t_cal tokens).
     """
     _check_codes(kv, layout, "kv")
     _check_codes(mu, layout, "mu")
@@ -280,8 +313,7 @@ def calibrate_sigma(layout: Layout, kv: torch.Tensor, mu: torch.Tensor, t_cal: i
         if not mask.is_cuda or not mask.is_contiguous() or mask.element_size() != 1 \
                 or mask.numel() != layout.n_elems:
             raise ValueError("mask must be a contiguous 1-byte CUDA tensor shaped like kv")
-    sigma = torch.empty((layout.n_layers, layout.n_kv, layout.n_heads, layout.head_dim),
-                        dtype=torch.float32, device=kv.device)
+    sigma = torch.empty(layout.sigma_shape, dtype=torch.float32, device=kv.device)
     rc = B.lib().skv_calibrate_sigma(C.byref(layout.c()), _ptr(kv), _ptr(mu), _ptr(mask), int(t_cal),
                                      _ptr(sigma), _stream_handle(stream))
     B.check("skv_calibrate_sigma", rc)

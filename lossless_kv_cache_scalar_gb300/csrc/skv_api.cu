@@ -33,8 +33,8 @@ __device__ uint32_t phat_entry(uint64_t cum, uint64_t total) {
     return p;
 }
 
-// One CTA: validates sigma and writes rsig = fl32(1/sigma); builds P_hat in
-// code order from the marginal histogram.
+// All CTAs validate sigma and write rsig = fl32(1/sigma) (grid-stride); CTA 0
+// also builds P_hat in code order from the marginal histogram.
 template <uint32_t DT>
 __global__ void __launch_bounds__(1024) setup_kernel(const SetupArgs a) {
     using K = Codes<DT>;
@@ -45,12 +45,17 @@ __global__ void __launch_bounds__(1024) setup_kernel(const SetupArgs a) {
     if (tid == 0) bad_sigma = 0;
     __syncthreads();
 
-    const uint64_t nsig = g.n_planes * g.HD;
-    for (uint64_t i = tid; i < nsig; i += blockDim.x) {
+    const uint64_t nsig = g.n_planes * g.n_sblk * g.HD;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + tid; i < nsig; i += (uint64_t)gridDim.x * blockDim.x) {
         const float sg = a.sigma[i];
         const bool ok = isfinite(sg) && sg >= 1.17549435e-38f;   // 2^-126
         a.rsig[i] = ok ? __frcp_rn(sg) : 1.0f;
         if (!ok) bad_sigma = 1;
+    }
+    if (blockIdx.x != 0) {
+        __syncthreads();
+        if (tid == 0 && bad_sigma) set_status(a.status, SKV_ERR_BAD_SIGMA);
+        return;
     }
 
     if (g.w_h == 0) {
@@ -138,10 +143,11 @@ __global__ void __launch_bounds__(256) cdf_eval_kernel(const CdfArgs a) {
 static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 static int32_t make_geom(const skv_layout *lay, Geom &g) {
-    if (!lay || lay->version != SKV_FORMAT_VERSION || lay->reserved != 0) return SKV_ERR_INVALID_ARG;
+    if (!lay || lay->version != SKV_FORMAT_VERSION) return SKV_ERR_INVALID_ARG;
     if (lay->dtype != SKV_BF16 && lay->dtype != SKV_E4M3) return SKV_ERR_INVALID_ARG;
     if (!lay->n_layers || !lay->n_kv || !lay->n_heads || !lay->head_dim) return SKV_ERR_INVALID_ARG;
     if (!lay->tokens_per_chunk) return SKV_ERR_INVALID_ARG;
+    if (lay->sigma_block_tokens % lay->tokens_per_chunk != 0) return SKV_ERR_INVALID_ARG;
     const uint32_t W = lay->streams_per_chunk;
     if (W == 0 || W % 32 != 0 || W > 256) return SKV_ERR_INVALID_ARG;
     if (lay->w_narrow + lay->w_wide + lay->w_marginal != 100u) return SKV_ERR_INVALID_ARG;
@@ -160,6 +166,8 @@ static int32_t make_geom(const skv_layout *lay, Geom &g) {
     g.P = (lay->n_tokens + lay->tokens_per_chunk - 1) / lay->tokens_per_chunk;
     g.n_planes = (uint64_t)lay->n_layers * lay->n_kv;
     g.n_chunks = g.n_planes * g.P;
+    g.SB = lay->sigma_block_tokens;
+    g.n_sblk = g.SB ? (g.T + g.SB - 1) / g.SB : 1;
     g.n_groups = g.n_chunks * g.G;
     g.w_n = lay->w_narrow;
     g.w_w = lay->w_wide;
@@ -211,7 +219,7 @@ static Workspace carve(const Geom &g, int kind, uint8_t *base) {
     o_phat = off;
     off += round256(4ull * (d.N + 1));
     o_rsig = off;
-    off += round256(4ull * g.n_planes * g.HD);
+    off += round256(4ull * g.n_planes * g.n_sblk * g.HD);
     uint64_t o_ep = 0;
     if (kind == WS_ENCODE && g.dtype == SKV_BF16) {
         o_ep = off;
@@ -258,8 +266,11 @@ static Workspace carve(const Geom &g, int kind, uint8_t *base) {
 static int32_t run_setup(const Geom &g, const float *sigma, const uint64_t *counts,
                          const Workspace &ws, int32_t *status, cudaStream_t st) {
     SetupArgs s{g, sigma, counts, ws.phat, ws.rsig, ws.ep, status};
-    if (g.dtype == SKV_BF16) setup_kernel<SKV_BF16><<<1, 1024, 0, st>>>(s);
-    else setup_kernel<SKV_E4M3><<<1, 1024, 0, st>>>(s);
+    // one CTA per 64 Ki sigmas beyond the first (CTA 0 also builds P_hat)
+    const uint64_t nsig = g.n_planes * g.n_sblk * g.HD;
+    const unsigned grid = (unsigned)(1 + (nsig > 65536 ? (nsig - 65536 + 65535) / 65536 : 0));
+    if (g.dtype == SKV_BF16) setup_kernel<SKV_BF16><<<grid < 1024 ? grid : 1024, 1024, 0, st>>>(s);
+    else setup_kernel<SKV_E4M3><<<grid < 1024 ? grid : 1024, 1024, 0, st>>>(s);
     return cudaGetLastError() == cudaSuccess ? SKV_OK : SKV_ERR_CUDA;
 }
 
@@ -523,7 +534,8 @@ int32_t skv_calibrate_sigma(const skv_layout *lay, const void *kv, const void *m
     Geom g;
     int32_t r = make_geom(lay, g);
     if (r != SKV_OK) return r;
-    if (t_cal == 0 || t_cal > g.T || !kv || !mu || !sigma) return SKV_ERR_INVALID_ARG;
+    if (t_cal == 0 || t_cal > g.T || (g.SB && t_cal > g.SB) || !kv || !mu || !sigma)
+        return SKV_ERR_INVALID_ARG;
     const uint32_t b = dtype_info(g.dtype).bytes;
     if (((uintptr_t)kv % b) != 0 || ((uintptr_t)mu % b) != 0 || ((uintptr_t)sigma & 3u) != 0)
         return SKV_ERR_INVALID_ARG;

@@ -117,9 +117,10 @@ __global__ void __launch_bounds__(kHist8Warps * 32) hist_e4m3_kernel(const uint8
 
 // -------------------------------------------------------- sigma calibration
 
-// One thread per (plane, channel); consecutive threads take consecutive
-// channels, so each token row is read coalesced. Over tokens t < t_cal, in
-// ascending order, an element counts when its KV and mu codes are both finite
+// One thread per (plane, sigma block, channel); consecutive threads take
+// consecutive channels, so each token row is read coalesced. Over the first
+// t_cal tokens of the block (the plane's first t_cal tokens without sigma
+// blocks), in ascending order, an element counts when its KV and mu codes are both finite
 // and its mask byte (if a mask is given) is nonzero:
 //     r = fl64(value(kv) - value(mu)),  S = S + fl64(r * r)  (binary64 throughout)
 //     sigma = fl32(sqrt(fl64(S / n_counted)))
@@ -166,20 +167,23 @@ __global__ void __launch_bounds__(kCalibThreads) calib_kernel(const CalibArgs a)
     using K = Codes<DT>;
     const Geom &g = a.g;
     const uint64_t id = (uint64_t)blockIdx.x * kCalibThreads + threadIdx.x;
-    if (id >= g.n_planes * g.HD) return;
-    const uint64_t plane = id / g.HD, c = id % g.HD;
-    const uint64_t e0 = plane * g.T * g.HD + c;           // element of token 0
+    if (id >= g.n_planes * g.n_sblk * g.HD) return;
+    const uint64_t row = id / g.HD, c = id % g.HD;        // row = plane * n_sblk + block
+    const uint64_t plane = row / g.n_sblk, blk = row % g.n_sblk;
+    const uint64_t t_first = blk * g.SB;                  // 0 without sigma blocks
+    const uint64_t t_cal = a.t_cal < g.T - t_first ? a.t_cal : g.T - t_first;
+    const uint64_t e0 = (plane * g.T + t_first) * g.HD + c;   // element of the first token
     auto load = [&](const uint8_t *p, uint64_t el) -> uint32_t {
         return K::bytes == 2 ? __ldg(reinterpret_cast<const uint16_t *>(p) + el) : __ldg(p + el);
     };
     double S = 0.0;
     uint64_t cnt = 0;
-    for (uint64_t t0 = 0; t0 < a.t_cal; t0 += kCalibBatch) {
+    for (uint64_t t0 = 0; t0 < t_cal; t0 += kCalibBatch) {
         uint32_t kb[kCalibBatch], mb[kCalibBatch], keep[kCalibBatch];
 #pragma unroll
         for (int i = 0; i < kCalibBatch; ++i) {
             const uint64_t t = t0 + i;
-            const bool in = t < a.t_cal;
+            const bool in = t < t_cal;
             const uint64_t el = e0 + (in ? t : 0) * g.HD;
             kb[i] = load(a.kv, el);
             mb[i] = load(a.mu, el);
@@ -230,7 +234,7 @@ int launch_histogram(uint32_t dtype, const void *codes, uint64_t n, unsigned lon
 
 int launch_calibrate(const Geom &g, const void *kv, const void *mu, const uint8_t *mask,
                      uint64_t t_cal, float *sigma, cudaStream_t st) {
-    const uint64_t threads = g.n_planes * g.HD;
+    const uint64_t threads = g.n_planes * g.n_sblk * g.HD;
     const uint64_t blocks = (threads + kCalibThreads - 1) / kCalibThreads;
     if (blocks == 0) return 0;
     const CalibArgs ca{g, static_cast<const uint8_t *>(kv), static_cast<const uint8_t *>(mu), mask,

@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 4) decode_kernel(const DecArgs
     const int64_t nq = (int64_t)stream_vectors(g, cs.n_vec, s);
     const int64_t nq0 = (int64_t)stream_vectors(g, cs.n_vec, grp * 32u);
     const uint8_t *mup = a.mu + cs.elem0 * K::bytes;
-    const float *rsp = a.rsig + cs.plane * g.HD;
+    const float *rsp = a.rsig + sigma_row(g, k) * g.HD;
     uint8_t *outp = a.ids ? a.out + unit * a.page_elems * K::bytes : a.out + cs.elem0 * K::bytes;
     const float kS = (float)(100.0 * 16777216.0 / (double)((1u << m) - K::N));
     const float inv_total = (g.w_n + g.w_w) ? 1.0f / ((float)(g.w_n + g.w_w) * 16777216.0f) : 0.0f;

@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(kEncWarps * 32, 3) encode_kernel(const EncArgs
     const int64_t nq0 = (int64_t)stream_vectors(g, cs.n_vec, grp * 32u);
     const uint8_t *kvp = a.kv + cs.elem0 * K::bytes;
     const uint8_t *mup = a.mu + cs.elem0 * K::bytes;
-    const float *rsp = a.rsig + cs.plane * g.HD;
+    const float *rsp = a.rsig + sigma_row(g, k) * g.HD;
     uint32_t *slot = a.scratch + gid * g.cap_words;
     const Weights w{g.w_n, g.w_w, g.w_h};
     const uint32_t lt = lanemask_lt();

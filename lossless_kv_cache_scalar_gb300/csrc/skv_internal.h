@@ -37,6 +37,8 @@ struct Geom {
     uint64_t n_chunks;
     uint64_t n_groups;     // n_chunks * G
     uint64_t n_planes;     // n_layers * n_kv
+    uint64_t SB;           // sigma block tokens (0: one sigma row per plane)
+    uint64_t n_sblk;       // sigma rows per plane
     uint32_t w_n, w_w, w_h;
     uint32_t hdr_bytes;    // 8 W + pad16(4 G)
     uint64_t cap_words;    // scratch words per group (encoder)
@@ -61,6 +63,14 @@ SKV_HD ChunkSpan chunk_span(const Geom &g, uint64_t k) {
     c.elem0 = (c.plane * g.T + tok0) * g.HD;
     c.n_vec = ntok * g.HD / dtype_info(g.dtype).V;
     return c;
+}
+
+// Row of the sigma table (HD entries) that chunk k reads: its plane's row, or
+// with sigma blocks the row of the block holding its page (a block is a
+// whole number of pages, so one row serves the whole chunk).
+SKV_HD uint64_t sigma_row(const Geom &g, uint64_t k) {
+    const uint64_t plane = k / g.P, page = k % g.P;
+    return plane * g.n_sblk + (g.SB ? page * g.Tc / g.SB : 0);
 }
 
 // Number of vectors owned by stream s of a chunk with n_vec vectors.

@@ -35,7 +35,8 @@ class _Layout(C.Structure):
     _fields_ = [("dtype", C.c_uint32), ("n_layers", C.c_uint32), ("n_kv", C.c_uint32),
                 ("n_heads", C.c_uint32), ("head_dim", C.c_uint32), ("n_tokens", C.c_uint64),
                 ("tokens_per_chunk", C.c_uint32), ("streams_per_chunk", C.c_uint32),
-                ("w_n", C.c_uint32), ("w_w", C.c_uint32), ("w_h", C.c_uint32)]
+                ("w_n", C.c_uint32), ("w_w", C.c_uint32), ("w_h", C.c_uint32),
+                ("sigma_block", C.c_uint32)]
 
 
 @dataclass
@@ -51,11 +52,22 @@ class Layout:
     w_n: int = 95
     w_w: int = 3
     w_h: int = 2
+    sigma_block: int = 0       # tokens per sigma block (0: one sigma per channel)
 
     def c(self) -> _Layout:
         return _Layout(self.dtype, self.n_layers, self.n_kv, self.n_heads, self.head_dim,
                        self.n_tokens, self.tokens_per_chunk, self.streams_per_chunk,
-                       self.w_n, self.w_w, self.w_h)
+                       self.w_n, self.w_w, self.w_h, self.sigma_block)
+
+    @property
+    def n_sigma_blocks(self) -> int:
+        return -(-self.n_tokens // self.sigma_block) if self.sigma_block else 1
+
+    @property
+    def sigma_shape(self) -> tuple:
+        if self.sigma_block:
+            return (self.n_layers, self.n_kv, self.n_sigma_blocks, self.n_heads, self.head_dim)
+        return (self.n_layers, self.n_kv, self.n_heads, self.head_dim)
 
     @property
     def n_codes(self) -> int:
@@ -207,6 +219,10 @@ def _inputs(lay, kv, mu, sigma, counts):
     kv = None if kv is None else np.ascontiguousarray(kv).view(cd).reshape(-1)
     mu = np.ascontiguousarray(mu).view(cd).reshape(-1)
     sigma = np.ascontiguousarray(sigma, np.float32).reshape(-1)
+    if sigma.size != int(np.prod(lay.sigma_shape)):
+        raise ValueError(f"sigma has {sigma.size} entries, the layout needs {lay.sigma_shape}")
+    if mu.size != lay.n_elems or (kv is not None and kv.size != lay.n_elems):
+        raise ValueError("kv / mu sizes do not match the layout")
     counts = _counts_arg(lay.dtype, counts)
     return kv, mu, sigma, counts
 
@@ -279,13 +295,14 @@ def histogram(dtype: int, codes, counts=None) -> np.ndarray:
 
 def calibrate_sigma(lay: Layout, kv: np.ndarray, mu: np.ndarray, t_cal: int,
                     mask: np.ndarray | None = None) -> np.ndarray:
-    """Frozen per-channel sigma (float32 [n_layers][n_kv][H][D]) from tokens < t_cal."""
+    """Frozen per-channel sigma (float32 [n_layers][n_kv][H][D], or per sigma block
+    [n_layers][n_kv][n_blocks][H][D]) from the first t_cal tokens (of each block)."""
     cd = lay.code_dtype
     kv = np.ascontiguousarray(kv).view(cd)
     mu = np.ascontiguousarray(mu).view(cd)
     if mask is not None:
         mask = np.ascontiguousarray(mask).view(np.uint8)
-    out = np.zeros((lay.n_layers, lay.n_kv, lay.n_heads, lay.head_dim), np.float32)
+    out = np.zeros(lay.sigma_shape, np.float32)
     _check(lib().oracle_calibrate_sigma(C.byref(lay.c()), _p(kv), _p(mu), _p(mask), int(t_cal),
                                         _p(out)))
     return out

@@ -57,6 +57,7 @@ typedef struct {
     uint64_t n_tokens;
     uint32_t tokens_per_chunk, streams_per_chunk;
     uint32_t w_n, w_w, w_h;
+    uint32_t sigma_block;  /* 0: one sigma per channel; else tokens per sigma block */
 } or_layout;
 
 typedef struct {          /* per-dtype constants, FORMAT.md section 1 */
@@ -302,6 +303,7 @@ typedef struct {
     or_layout lay;
     or_dtype d;
     uint64_t HD, P, n_chunks;
+    uint64_t n_sblk;       /* sigma rows per (layer, kv) plane */
     uint32_t W, G;
 } or_geom;
 
@@ -311,6 +313,7 @@ static int geom_init(const or_layout *lay, or_geom *g)
     if (lay->n_layers == 0 || lay->n_kv == 0 || lay->n_heads == 0 || lay->head_dim == 0)
         return OR_ERR_INVALID_ARG;
     if (lay->tokens_per_chunk == 0) return OR_ERR_INVALID_ARG;
+    if (lay->sigma_block % lay->tokens_per_chunk != 0) return OR_ERR_INVALID_ARG;
     if (lay->streams_per_chunk == 0 || lay->streams_per_chunk % 32 != 0 ||
         lay->streams_per_chunk > 256) return OR_ERR_INVALID_ARG;
     if (lay->w_n + lay->w_w + lay->w_h != 100) return OR_ERR_INVALID_ARG;
@@ -322,7 +325,21 @@ static int geom_init(const or_layout *lay, or_geom *g)
     g->n_chunks = (uint64_t)lay->n_layers * lay->n_kv * g->P;
     g->W = lay->streams_per_chunk;
     g->G = g->W / 32;
+    g->n_sblk = lay->sigma_block ? (lay->n_tokens + lay->sigma_block - 1) / lay->sigma_block : 1;
     return OR_OK;
+}
+
+/* FORMAT.md section 4: the sigma entry of global element i. Without sigma
+   blocks it is the element's (layer, kv, channel); with blocks of B tokens
+   also its token's block t / B. */
+static uint64_t sigma_index(const or_geom *g, uint64_t i)
+{
+    uint64_t T = g->lay.n_tokens;
+    uint64_t plane = i / (T * g->HD);
+    uint64_t t = (i / g->HD) % T;
+    uint64_t c = i % g->HD;
+    uint64_t blk = g->lay.sigma_block ? t / g->lay.sigma_block : 0;
+    return (plane * g->n_sblk + blk) * g->HD + c;
 }
 
 /* Chunk k: first element (global index), its (layer, kv) plane, vector count. */
@@ -436,7 +453,7 @@ typedef struct {
     const or_geom *g;
     const or_model *md;
     const void *kv, *mu;
-    const float *rs_all;       /* fl32(1/sigma), [plane][HD] */
+    const float *rs_all;       /* fl32(1/sigma), one per sigma entry */
     int bad_mu;
 } or_ctx;
 
@@ -448,7 +465,6 @@ static uint64_t encode_chunk(or_ctx *cx, uint64_t k, uint8_t *buf)
     const uint64_t M = 1ull << m, L = 1ull << (m + 7);
     uint64_t e0, plane, n_vec;
     chunk_span(g, k, &e0, &plane, &n_vec);
-    const float *rs = cx->rs_all + plane * g->HD;
 
     uint64_t hdr = header_bytes(g);
     memset(buf, 0, hdr);
@@ -471,7 +487,7 @@ static uint64_t encode_chunk(or_ctx *cx, uint64_t k, uint8_t *buf)
                 uint64_t el = stream_elem(g, s, i);
                 uint32_t code = load_code(g, cx->kv, e0 + el);
                 float mu = mu_value(g->lay.dtype, load_code(g, cx->mu, e0 + el), &cx->bad_mu);
-                float r = rs[el % g->HD];
+                float r = cx->rs_all[sigma_index(g, e0 + el)];
                 uint32_t o = oracle_ord(g->lay.dtype, code);
                 uint64_t c = cdf_at(cx->md, o, mu, r);
                 uint64_t f = cdf_at(cx->md, o + 1, mu, r) - c;
@@ -512,7 +528,6 @@ static int decode_chunk(or_ctx *cx, uint64_t k, const uint8_t *buf, uint64_t siz
     const uint64_t M = 1ull << m, L = 1ull << (m + 7);
     uint64_t e0, plane, n_vec;
     chunk_span(g, k, &e0, &plane, &n_vec);
-    const float *rs = cx->rs_all + plane * g->HD;
 
     uint64_t hdr = header_bytes(g);
     if (size < hdr) return OR_ERR_CORRUPT;
@@ -539,7 +554,7 @@ static int decode_chunk(or_ctx *cx, uint64_t k, const uint8_t *buf, uint64_t siz
                 uint32_t s = 32 * grp + l;
                 uint64_t el = stream_elem(g, s, i);
                 float mu = mu_value(g->lay.dtype, load_code(g, cx->mu, e0 + el), &cx->bad_mu);
-                float r = rs[el % g->HD];
+                float r = cx->rs_all[sigma_index(g, e0 + el)];
                 uint64_t slot = x[l] & (M - 1);
                 uint32_t o = find_symbol(cx->md, slot, mu, r);
                 uint64_t c = cdf_at(cx->md, o, mu, r);
@@ -582,7 +597,7 @@ static int setup_init(const or_layout *lay, const float *sigma, const uint64_t *
     int st = geom_init(lay, &su->g);
     if (st) return st;
     su->P = malloc(sizeof(uint32_t) * (su->g.d.N + 1));
-    uint64_t nsig = (uint64_t)lay->n_layers * lay->n_kv * su->g.HD;
+    uint64_t nsig = (uint64_t)lay->n_layers * lay->n_kv * su->g.n_sblk * su->g.HD;
     su->rs = malloc(sizeof(float) * (nsig ? nsig : 1));
     if (!su->P || !su->rs) { setup_free(su); return OR_ERR_NOMEM; }
     for (uint64_t i = 0; i < nsig; i++) {
@@ -809,9 +824,7 @@ double oracle_ideal_bits(const or_layout *lay, const void *kv, const void *mu,
     uint64_t n_el = (uint64_t)lay->n_layers * lay->n_kv * lay->n_tokens * g.HD;
     double bits = 0.0;
     for (uint64_t i = 0; i < n_el; i++) {
-        uint64_t plane = i / (lay->n_tokens * g.HD);
-        uint64_t ch = i % g.HD;
-        double s = sigma[plane * g.HD + ch];
+        double s = sigma[sigma_index(&g, i)];
         uint32_t code = load_code(&g, kv, i);
         uint32_t mc = load_code(&g, mu, i);
         double m = code_is_finite(lay->dtype, mc) ? oracle_value(lay->dtype, mc) : 0.0;
@@ -838,8 +851,7 @@ double oracle_model_bits(const or_layout *lay, const void *kv, const void *mu,
     double bits = 0.0, M = (double)(1ull << su.g.d.m);
     int bad = 0;
     for (uint64_t i = 0; i < n_el; i++) {
-        uint64_t plane = i / (lay->n_tokens * su.g.HD);
-        float r = su.rs[plane * su.g.HD + i % su.g.HD];
+        float r = su.rs[sigma_index(&su.g, i)];
         uint32_t code = load_code(&su.g, kv, i);
         float m = mu_value(lay->dtype, load_code(&su.g, mu, i), &bad);
         uint32_t o = oracle_ord(lay->dtype, code);
@@ -880,7 +892,9 @@ int oracle_histogram(uint32_t dtype, const void *codes, uint64_t n, uint64_t *co
  * counted elements (both codes finite; mask byte nonzero when a mask is
  * given), summed in binary64 in token order and rounded to binary32 at the
  * end, then clamped into the valid range [2^-126, FLT_MAX] (2^-126 when
- * nothing is counted).
+ * nothing is counted). With sigma blocks of B tokens (the position-aware
+ * sigma the blog's limitations section names), each block gets its own sigma
+ * from its own first t_cal tokens (t_cal <= B; a short last block uses all).
  */
 int oracle_calibrate_sigma(const or_layout *lay, const void *kv, const void *mu,
                            const uint8_t *mask, uint64_t t_cal, float *sigma)
@@ -889,27 +903,33 @@ int oracle_calibrate_sigma(const or_layout *lay, const void *kv, const void *mu,
     int st = geom_init(lay, &g);
     if (st != OR_OK) return st;
     if (t_cal == 0 || t_cal > lay->n_tokens || !kv || !mu || !sigma) return OR_ERR_INVALID_ARG;
+    if (lay->sigma_block && t_cal > lay->sigma_block) return OR_ERR_INVALID_ARG;
     uint64_t planes = (uint64_t)lay->n_layers * lay->n_kv;
+    uint64_t B = lay->sigma_block ? lay->sigma_block : lay->n_tokens;
     for (uint64_t p = 0; p < planes; ++p) {
-        for (uint64_t c = 0; c < g.HD; ++c) {
-            double S = 0.0;
-            uint64_t count = 0;
-            for (uint64_t t = 0; t < t_cal; ++t) {
-                uint64_t el = (p * lay->n_tokens + t) * g.HD + c;
-                if (mask && mask[el] == 0) continue;
-                uint32_t kb = load_code(&g, kv, el), mb = load_code(&g, mu, el);
-                if (!code_is_finite(lay->dtype, kb) || !code_is_finite(lay->dtype, mb)) continue;
-                double r = (double)oracle_value(lay->dtype, kb) - (double)oracle_value(lay->dtype, mb);
-                S += r * r;
-                count += 1;
+        for (uint64_t b = 0; b < g.n_sblk; ++b) {
+            uint64_t t0 = b * B;
+            uint64_t t1 = t0 + t_cal < lay->n_tokens ? t0 + t_cal : lay->n_tokens;
+            for (uint64_t c = 0; c < g.HD; ++c) {
+                double S = 0.0;
+                uint64_t count = 0;
+                for (uint64_t t = t0; t < t1; ++t) {
+                    uint64_t el = (p * lay->n_tokens + t) * g.HD + c;
+                    if (mask && mask[el] == 0) continue;
+                    uint32_t kb = load_code(&g, kv, el), mb = load_code(&g, mu, el);
+                    if (!code_is_finite(lay->dtype, kb) || !code_is_finite(lay->dtype, mb)) continue;
+                    double r = (double)oracle_value(lay->dtype, kb) - (double)oracle_value(lay->dtype, mb);
+                    S += r * r;
+                    count += 1;
+                }
+                float s = 0x1p-126f;
+                if (count) {
+                    s = (float)sqrt(S / (double)count);
+                    if (!(s >= 0x1p-126f)) s = 0x1p-126f;
+                    if (s > 0x1.fffffep127f) s = 0x1.fffffep127f;
+                }
+                sigma[(p * g.n_sblk + b) * g.HD + c] = s;
             }
-            float s = 0x1p-126f;
-            if (count) {
-                s = (float)sqrt(S / (double)count);
-                if (!(s >= 0x1p-126f)) s = 0x1p-126f;
-                if (s > 0x1.fffffep127f) s = 0x1.fffffep127f;
-            }
-            sigma[p * g.HD + c] = s;
         }
     }
     return OR_OK;

@@ -50,7 +50,7 @@ def test_layout_init_and_checks():
     assert (lay.tokens_per_chunk, lay.streams_per_chunk) == (256, 64)
     assert (lay.w_narrow, lay.w_wide, lay.w_marginal) == (95, 3, 2)
     bad = [dict(streams_per_chunk=48), dict(streams_per_chunk=288), dict(tokens_per_chunk=0),
-           dict(w_marginal=3), dict(version=2), dict(dtype=5), dict(n_heads=1, head_dim=4), dict(reserved=1)]
+           dict(w_marginal=3), dict(version=2), dict(dtype=5), dict(n_heads=1, head_dim=4), dict(sigma_block_tokens=100)]
     for kw in bad:
         l2 = B.skv_layout()
         C.memmove(C.byref(l2), C.byref(lay), C.sizeof(lay))

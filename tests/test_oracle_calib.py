@@ -170,3 +170,76 @@ def test_sigma_matches_generator_calibration(name):
     s = O.calibrate_sigma(lay, h["kv"], h["mu"], cfg.calib_tokens, mask=mask)
     ulps = np.abs(s.view(np.int32).astype(np.int64) - h["sigma"].view(np.int32).astype(np.int64))
     assert ulps.max() <= 1
+
+
+# ------------------------------------------------------------ sigma blocks
+
+def _encode_chunks(lay, kv, mu, sigma, counts):
+    stream, offs = O.encode(lay, kv, mu, sigma, counts)
+    return [bytes(stream[offs[k]:offs[k + 1]]) for k in range(len(offs) - 1)]
+
+
+@pytest.mark.parametrize("dtype", [O.BF16, O.E4M3])
+def test_sigma_blocks_equal_per_block_static_coding(dtype):
+    """A cache coded with one sigma per block of B tokens gives, chunk for
+    chunk, the bytes of each block's tokens coded as a cache of its own with
+    that block's sigma as the frozen sigma (chunks are independent, and a
+    block is a whole number of pages)."""
+    H_, D = (2, 8) if dtype == O.BF16 else (1, 16)
+    L, K, T, Tc, B = 2, 2, 700, 100, 300        # blocks of 300, 300, 100 tokens
+    lay = O.Layout(dtype, L, K, H_, D, T, Tc, 32, sigma_block=B)
+    rng = np.random.default_rng(21)
+    cd = lay.code_dtype
+    n = 65536 if dtype == O.BF16 else 256
+    lo, hi = (0x3C00, 0x4100) if dtype == O.BF16 else (0x30, 0x50)
+    mu = rng.integers(lo, hi, (L, K, T, H_, D)).astype(cd)
+    kv = (mu.astype(np.int32) + rng.integers(-20, 21, mu.shape)).astype(cd)
+    sigma = (0.01 + rng.random(lay.sigma_shape)).astype(np.float32)
+    counts = O.histogram(dtype, kv)
+    got = _encode_chunks(lay, kv, mu, sigma, counts)
+    P = -(-T // Tc)
+    for b in range(lay.n_sigma_blocks):
+        t0, t1 = b * B, min(T, (b + 1) * B)
+        sub = O.Layout(dtype, L, K, H_, D, t1 - t0, Tc, 32)
+        ref = _encode_chunks(sub, np.ascontiguousarray(kv[:, :, t0:t1]),
+                             np.ascontiguousarray(mu[:, :, t0:t1]),
+                             np.ascontiguousarray(sigma[:, :, b]), counts)
+        Pb = -(-(t1 - t0) // Tc)
+        for p in range(L * K):
+            for j in range(Pb):
+                assert got[p * P + t0 // Tc + j] == ref[p * Pb + j], (b, p, j)
+    # and the whole cache decodes back
+    stream, offs = O.encode(lay, kv, mu, sigma, counts)
+    assert np.array_equal(O.decode(lay, stream, offs, mu, sigma, counts), kv.reshape(-1))
+    # a sigma table of the wrong shape is refused before the C code reads it
+    with pytest.raises(ValueError):
+        O.encode(lay, kv, mu, sigma[:, :, :2], counts)
+
+
+def test_sigma_blocks_calibration():
+    """Each block's sigma is its own first t_cal tokens' RMS: block 0 holds
+    residuals 1 and 7 (sigma 5), block 1 residual 3 (sigma 3), and the short
+    last block residual 0.5 (sigma 0.5) -- and equals the static calibration
+    of the block's tokens alone."""
+    lay = O.Layout(O.BF16, 1, 2, 2, 8, 600, 100, 32, sigma_block=200)
+    shape = (1, 2, 600, 2, 8)
+    mu = np.zeros(shape, np.uint16)
+    kv = np.full(shape, BF16_ONE, np.uint16)
+    kv[:, :, 1:200:2] = BF16_SEVEN
+    kv[:, :, 200:400] = 0x4040                      # 3.0
+    kv[:, :, 400:] = 0x3F00                         # 0.5
+    s = O.calibrate_sigma(lay, kv, mu, t_cal=200)
+    assert s.shape == (1, 2, 3, 2, 8)
+    assert np.all(s[:, :, 0] == 5.0) and np.all(s[:, :, 1] == 3.0) and np.all(s[:, :, 2] == 0.5)
+    rng = np.random.default_rng(4)
+    kv2, mu2 = _random_pair(O.Layout(O.BF16, 1, 2, 2, 8, 600), 8)
+    s2 = O.calibrate_sigma(lay, kv2, mu2, t_cal=150)
+    for b in range(3):
+        sub = O.Layout(O.BF16, 1, 2, 2, 8, 200)
+        ref = O.calibrate_sigma(sub, np.ascontiguousarray(kv2[:, :, 200 * b:200 * (b + 1)]),
+                                np.ascontiguousarray(mu2[:, :, 200 * b:200 * (b + 1)]), t_cal=150)
+        assert np.array_equal(s2[:, :, b], ref)
+    with pytest.raises(O.OracleError):
+        O.calibrate_sigma(lay, kv2, mu2, t_cal=201)
+    with pytest.raises(O.OracleError):          # B must be a multiple of the page length
+        O.calibrate_sigma(O.Layout(O.BF16, 1, 2, 2, 8, 600, 100, 32, sigma_block=150), kv2, mu2, 10)
