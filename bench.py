@@ -172,6 +172,9 @@ def main():
     ap.add_argument("--sigma-block", type=int, default=0,
                     help="tokens per sigma block (0: the workload's frozen per-channel sigma); "
                          "blocks are calibrated on the device from their own tokens")
+    ap.add_argument("--offload", type=int, default=1,
+                    help="time the offload decode from pinned host memory (0: skip)")
+    ap.add_argument("--staging-mb", type=int, default=1024, help="offload staging buffer (two halves)")
     ap.add_argument("--model-inputs", type=int, default=1,
                     help="time skv_histogram and skv_calibrate_sigma on the workload (0: skip)")
     ap.add_argument("--traffic-json", default=os.path.join(ROOT, "profiles", "traffic.json"))
@@ -268,6 +271,7 @@ def main():
     hbm_peak = _peaks().get("hbm_gbs", 6685.5)
     page_lat = page_latency(coder, out, offsets, w, lay, args, dev) if args.page_latency else None
     inputs = model_inputs_run(w, lay, args, dev, hbm_peak) if args.model_inputs else None
+    offload = offload_run(coder, out, offsets, w, lay, args, dev, total_bytes) if args.offload else None
     bits = 8.0 * total_bytes / n_el
 
     # end to end through the public API with host buffers
@@ -311,6 +315,7 @@ def main():
             "cpu_baseline": cpu,
             "page_decode_latency_us": page_lat,
             "model_inputs": inputs,
+            "offload": offload,
             "e2e": e2e,
             "gpu_launches": 8 * args.steps,
             "clocks": clocks,
@@ -392,6 +397,73 @@ def model_inputs_run(w, lay, args, dev, hbm_peak, reps=5):
             "calibrate_bound": "fp64 pipe (3 binary64 ops per element; %d SMs)" % sms,
             "note": "histogram over all scalars (counts checked equal to the workload's); "
                     "sigma from tokens < %d without a mask; median of %d calls" % (t_cal, reps)}
+
+
+def offload_run(coder, out, offsets, w, lay, args, dev, total_bytes, reps=3):
+    """Decode the whole cache from a pinned host copy of its bitstream
+    (skv_decode_offload: batches copied on a second stream while the previous
+    batch decodes), against the host link itself: a pinned host-to-device copy
+    of the compressed bytes, and of the uncompressed KV (what offloading the
+    raw cache would move). Median of `reps` runs, CUDA events; 2 untimed first."""
+    stream = torch.cuda.Stream(device=dev)
+    copy_stream = torch.cuda.Stream(device=dev)
+    host = torch.empty(total_bytes, dtype=torch.uint8).pin_memory()
+    host.copy_(out[:total_bytes])
+    host_offs = offsets.cpu()
+    staging = torch.empty(args.staging_mb << 20, dtype=torch.uint8, device=dev)
+    back = torch.empty_like(w["kv"])
+    raw_bytes = lay.n_elems * lay.bytes_per_code
+    kv_host = torch.empty(raw_bytes, dtype=torch.uint8).pin_memory()
+    kv_dev = torch.empty(raw_bytes, dtype=torch.uint8, device=dev)
+    comp_dev = torch.empty(total_bytes, dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        ts = []
+        for i in range(2 + reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            copy_stream.wait_stream(stream)
+            fn()
+            stream.wait_stream(copy_stream)
+            e1.record(stream)
+            stream.synchronize()
+            if i >= 2:
+                ts.append(e0.elapsed_time(e1) / 1e3)
+        return float(np.median(ts))
+
+    t_off = timed(lambda: coder.decode_offload_into(host, host_offs, offsets, w["mu"], w["sigma"],
+                                                    w["counts"], back, staging, stream, copy_stream))
+    coder.check_status("offload", stream)
+    if not torch.equal(back, w["kv"]):
+        raise SystemExit("bench: offload decode did not restore the input")
+
+    def h2d(dst, src):
+        with torch.cuda.stream(copy_stream):
+            dst.copy_(src, non_blocking=True)
+
+    t_comp = timed(lambda: h2d(comp_dev, host))
+    t_raw = timed(lambda: h2d(kv_dev, kv_host))
+    # the library's plan: halves of the staging buffer, batches of whole decoder waves
+    half = (staging.numel() // 2) & ~15
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    wave = max(1, sms * 32 // (lay.streams_per_chunk // 32))
+    per = max(1, half // max(1, total_bytes // lay.n_chunks) // wave) * wave
+    n_batches = len(offload_plan_host(host_offs, half, per)) - 1
+    dec_gbs = raw_bytes / t_off / 1e9
+    link_comp = total_bytes / t_comp / 1e9
+    link_raw = raw_bytes / t_raw / 1e9
+    return {"decode_gbs": dec_gbs, "link_compressed_gbs": link_comp, "link_raw_gbs": link_raw,
+            "kv_gbs_if_link_bound": link_comp * raw_bytes / total_bytes,
+            "decode_over_link_kv_rate": dec_gbs / (link_comp * raw_bytes / total_bytes),
+            "decode_over_raw_offload": dec_gbs / link_raw,
+            "staging_mb": args.staging_mb, "batches": n_batches,
+            "note": "GB/s of uncompressed KV for decode; link = pinned host-to-device copy of the "
+                    "compressed stream / of the raw KV; median of %d" % reps}
+
+
+def offload_plan_host(host_offs, batch_bytes, max_chunks):
+    from lossless_kv_cache_scalar_gb300.api import offload_plan
+    return offload_plan(host_offs.numpy(), batch_bytes, max_chunks)
 
 
 def e2e_run(coder, w, lay, args, dev, total_bytes):

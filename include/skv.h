@@ -214,6 +214,49 @@ int32_t skv_decode_chunks_prepared(const skv_layout *lay, const void *bitstream,
                                    void *stream);
 
 /*
+ * Decode a whole cache whose bitstream sits in host memory: the offload use of
+ * the wiki's uses section (KV kept compressed off the GPU and brought back
+ * over the host link). The chunks are copied in batches into two halves of a
+ * device staging buffer on copy_stream while the previous batch decodes on
+ * stream, so transfer and decode overlap; each batch is the longest run of
+ * whole chunks (in chunk order) whose bytes fit one half. The result is the
+ * same as skv_decode's on a device copy of the stream.
+ *  host_bitstream  host memory (page-locked, e.g. cudaHostAlloc, for the copies to
+ *                  overlap), bitstream_bytes bytes: the stream skv_encode wrote
+ *  host_offsets    host uint64[n_chunks + 1]: the offsets (used to plan the batches)
+ *  offsets         device uint64[n_chunks + 1]: the same values (read by the decoder)
+ *  staging         device, staging_bytes, 16-byte aligned; each half must hold the
+ *                  largest chunk (else SKV_ERR_INVALID_ARG). Halves large enough for
+ *                  a few hundred chunks keep every SM busy.
+ *  stream, copy_stream  decode and copy streams (cudaStream_t as void*), distinct
+ *                  for overlap; the call returns once everything is enqueued.
+ * Other arguments and device errors as skv_decode. Host-detected: offsets that
+ * are not ascending from 0 or pass bitstream_bytes return SKV_ERR_CORRUPT and
+ * nothing is enqueued. host_bitstream and staging must stay untouched until
+ * stream has finished.
+ */
+int32_t skv_decode_offload(const skv_layout *lay, const void *host_bitstream, uint64_t bitstream_bytes,
+                           const uint64_t *host_offsets, const uint64_t *offsets, const void *mu,
+                           const float *sigma, const uint64_t *counts, void *kv_out, int32_t *status,
+                           void *workspace, uint64_t ws_bytes, void *staging, uint64_t staging_bytes,
+                           void *stream, void *copy_stream);
+
+/*
+ * The batch plan skv_decode_offload follows (host only, no CUDA call): cut
+ * chunks 0..n_chunks-1 into runs of whole chunks of at most batch_bytes bytes
+ * and (if max_chunks > 0) at most max_chunks chunks each, in order, each run
+ * as long as it can be. skv_decode_offload takes max_chunks = a whole number
+ * of decoder waves (the chunks whose warps fit on the GPU at once). batch_first[i] = first chunk
+ * of batch i, batch_first[n_batches] = n_chunks; pass max_batches = 0 (and
+ * batch_first = NULL) to get only *n_batches. SKV_ERR_INVALID_ARG if a chunk
+ * is larger than batch_bytes or max_batches < n_batches + 1; SKV_ERR_CORRUPT
+ * if the offsets descend.
+ */
+int32_t skv_offload_plan(const uint64_t *host_offsets, uint64_t n_chunks, uint64_t batch_bytes,
+                         uint64_t max_chunks, uint64_t *batch_first, uint64_t max_batches,
+                         uint64_t *n_batches);
+
+/*
  * Evaluate the model's cumulative frequency C(o) (FORMAT.md section 5) for n
  * independent queries: C[i] = C(ords[i]) for predictor code mu_codes[i] and
  * scale sigmas[i], under the weights of lay and the marginal counts. For

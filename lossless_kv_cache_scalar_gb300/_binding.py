@@ -47,6 +47,9 @@ SIGNATURES = {
     "skv_decode_prepare": (_i32, [_LP, _vp, _vp, _vp, _vp, _u64, _vp]),
     "skv_decode_chunks_prepared": (_i32, [_LP, _vp, _u64, _vp, _vp, _vp, _u32, _vp, _vp, _vp, _u64, _vp]),
     "skv_histogram": (_i32, [_u32, _vp, _u64, _vp, _i32, _vp]),
+    "skv_decode_offload": (_i32, [_LP, _vp, _u64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _u64, _vp,
+                                  _u64, _vp, _vp]),
+    "skv_offload_plan": (_i32, [_vp, _u64, _u64, _u64, _vp, _u64, C.POINTER(_u64)]),
     "skv_calibrate_sigma": (_i32, [_LP, _vp, _vp, _vp, _u64, _vp, _vp]),
 }
 

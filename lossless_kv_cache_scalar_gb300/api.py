@@ -233,6 +233,35 @@ class Coder:
                                                 _stream_handle(stream))
         B.check("skv_decode_chunks_prepared", rc)
 
+    def decode_offload_into(self, host_bitstream, host_offsets, offsets, mu, sigma, counts, kv_out,
+                            staging, stream=None, copy_stream=None):
+        """Enqueue skv_decode_offload: decode from a (pinned) host bitstream through
+        a two-half device staging buffer, copies on `copy_stream` overlapping decode
+        on `stream`. host_offsets is the CPU int64 copy of `offsets`."""
+        lay = self.layout
+        if host_bitstream.is_cuda or host_offsets.is_cuda:
+            raise ValueError("host_bitstream and host_offsets must be CPU tensors")
+        if host_offsets.dtype != torch.int64 or host_offsets.numel() != self.n_chunks + 1 \
+                or not host_offsets.is_contiguous() or not host_bitstream.is_contiguous():
+            raise ValueError("host_offsets must be a contiguous int64 CPU tensor of n_chunks + 1")
+        if offsets.numel() != self.n_chunks + 1 or not offsets.is_cuda:
+            raise ValueError("offsets must be the device offsets (n_chunks + 1)")
+        if not staging.is_cuda or staging.dtype != torch.uint8 or not staging.is_contiguous():
+            raise ValueError("staging must be a contiguous uint8 CUDA tensor")
+        _check_codes(mu, lay, "mu")
+        _check_codes(kv_out, lay, "kv_out")
+        _check_model_inputs(lay, sigma, counts)
+        st = _stream_handle(stream)
+        cs = copy_stream if copy_stream is not None else torch.cuda.Stream(device=mu.device)
+        rc = B.lib().skv_decode_offload(C.byref(self._c), C.c_void_p(host_bitstream.data_ptr()),
+                                        host_bitstream.numel() * host_bitstream.element_size(),
+                                        C.c_void_p(host_offsets.data_ptr()), _ptr(offsets), _ptr(mu),
+                                        _ptr(sigma), _ptr(counts), _ptr(kv_out), _ptr(self.status),
+                                        _ptr(self.workspace), self.workspace.numel(), _ptr(staging),
+                                        staging.numel(), st, C.c_void_p(cs.cuda_stream))
+        B.check("skv_decode_offload", rc)
+        return cs
+
     def decode_chunks(self, bitstream, offsets, mu, sigma, counts, chunk_ids, stream=None):
         lay = self.layout
         pages = torch.zeros((chunk_ids.numel(), lay.page_elems), dtype=mu.dtype, device=mu.device)
@@ -318,3 +347,19 @@ def calibrate_sigma(layout: Layout, kv: torch.Tensor, mu: torch.Tensor, t_cal: i
                                      _ptr(sigma), _stream_handle(stream))
     B.check("skv_calibrate_sigma", rc)
     return sigma
+
+
+def offload_plan(host_offsets, batch_bytes: int, max_chunks: int = 0) -> list:
+    """skv_offload_plan: first chunk of each batch (plus n_chunks at the end)."""
+    import numpy as np
+    offs = np.ascontiguousarray(np.asarray(host_offsets), dtype=np.uint64)
+    n = offs.size - 1
+    nb = C.c_uint64()
+    p = offs.ctypes.data_as(C.c_void_p)
+    B.check("skv_offload_plan", B.lib().skv_offload_plan(p, n, batch_bytes, max_chunks, None, 0,
+                                                         C.byref(nb)))
+    out = np.zeros(nb.value + 1, np.uint64)
+    B.check("skv_offload_plan", B.lib().skv_offload_plan(p, n, batch_bytes, max_chunks,
+                                                         out.ctypes.data_as(C.c_void_p), out.size,
+                                                         C.byref(nb)))
+    return [int(v) for v in out]

@@ -3,6 +3,8 @@
 // table) and the launches of the encoder and decoder kernels.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cstdlib>
 #include <cstring>
 
 #include "skv_model.cuh"
@@ -404,7 +406,7 @@ static int32_t decode_launch(const Geom &g, const void *bitstream, uint64_t bits
     DecArgs da{g, static_cast<const uint8_t *>(bitstream), bitstream_bytes, offsets,
                static_cast<const uint8_t *>(mu), ws.phat, ws.rsig, ws.qt, ws.inv_lo, ws.inv_hi,
                pages ? ids : nullptr,
-               n_units, static_cast<uint8_t *>(out), (uint64_t)g.Tc * g.HD, status};
+               n_units, static_cast<uint8_t *>(out), (uint64_t)g.Tc * g.HD, status, 0, 0};
     return launch_decode(da, st) ? SKV_ERR_CUDA : SKV_OK;
 }
 
@@ -541,6 +543,104 @@ int32_t skv_calibrate_sigma(const skv_layout *lay, const void *kv, const void *m
         return SKV_ERR_INVALID_ARG;
     return launch_calibrate(g, kv, mu, mask, t_cal, sigma, static_cast<cudaStream_t>(stream))
                ? SKV_ERR_CUDA : SKV_OK;
+}
+
+int32_t skv_offload_plan(const uint64_t *host_offsets, uint64_t n_chunks, uint64_t batch_bytes,
+                         uint64_t max_chunks, uint64_t *batch_first, uint64_t max_batches,
+                         uint64_t *n_batches) {
+    if (!host_offsets || !n_batches || (max_batches && !batch_first)) return SKV_ERR_INVALID_ARG;
+    uint64_t nb = 0, first = 0;
+    while (first < n_chunks) {
+        // the longest run of whole chunks from `first` whose bytes fit one batch
+        uint64_t last = first;
+        while (last < n_chunks) {
+            const uint64_t a = host_offsets[last], b = host_offsets[last + 1];
+            if (b < a) return SKV_ERR_CORRUPT;
+            if (b - host_offsets[first] > batch_bytes) break;
+            if (max_chunks && last - first == max_chunks) break;
+            ++last;
+        }
+        if (last == first) return SKV_ERR_INVALID_ARG;   // one chunk is larger than a batch
+        if (nb < max_batches) batch_first[nb] = first;
+        ++nb;
+        first = last;
+    }
+    if (nb < max_batches) batch_first[nb] = n_chunks;
+    *n_batches = nb;
+    return nb + 1 > max_batches && max_batches ? SKV_ERR_INVALID_ARG : SKV_OK;
+}
+
+int32_t skv_decode_offload(const skv_layout *lay, const void *host_bitstream, uint64_t bitstream_bytes,
+                           const uint64_t *host_offsets, const uint64_t *offsets, const void *mu,
+                           const float *sigma, const uint64_t *counts, void *kv_out, int32_t *status,
+                           void *workspace, uint64_t ws_bytes, void *staging, uint64_t staging_bytes,
+                           void *stream, void *copy_stream) {
+    Geom g;
+    int32_t r = make_geom(lay, g);
+    if (r != SKV_OK) return r;
+    if ((r = common_checks(g, sigma, counts, status, workspace, ws_bytes, WS_DECODE_MIN)) != SKV_OK) return r;
+    if (g.n_chunks && (!host_bitstream || !host_offsets || !staging || !aligned16(staging)))
+        return SKV_ERR_INVALID_ARG;
+    if ((r = decode_args_check(g, staging, offsets, mu, nullptr, g.n_chunks, false, kv_out)) != SKV_OK)
+        return r;
+    if (g.n_chunks && (host_offsets[0] != 0 || host_offsets[g.n_chunks] > bitstream_bytes))
+        return SKV_ERR_CORRUPT;
+    // plan on the host: two staging halves, each batch a run of whole chunks.
+    // A batch is also cut at a whole number of decoder waves (the chunks whose
+    // warps are resident at once), so that no batch ends on a mostly empty wave.
+    const uint64_t half = (staging_bytes / 2) & ~uint64_t(15);
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return SKV_ERR_CUDA;
+    const uint64_t wave = std::max<uint64_t>(1, (uint64_t)sms * kDecResidentWarps / g.G);
+    const uint64_t mean = g.n_chunks ? std::max<uint64_t>(1, host_offsets[g.n_chunks] / g.n_chunks) : 1;
+    const uint64_t per_batch = std::max<uint64_t>(1, half / mean / wave) * wave;
+    uint64_t nb = 0;
+    if ((r = skv_offload_plan(host_offsets, g.n_chunks, half, per_batch, nullptr, 0, &nb)) != SKV_OK)
+        return r;
+    uint64_t *first = static_cast<uint64_t *>(std::malloc(sizeof(uint64_t) * (nb + 1)));
+    if (!first) return SKV_ERR_INVALID_ARG;
+    if ((r = skv_offload_plan(host_offsets, g.n_chunks, half, per_batch, first, nb + 1, &nb)) != SKV_OK) {
+        std::free(first);
+        return r;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaStream_t cs = static_cast<cudaStream_t>(copy_stream);
+    cudaEvent_t copied[2] = {nullptr, nullptr}, freed[2] = {nullptr, nullptr};
+    bool ok = true;
+    for (int h = 0; h < 2 && ok; ++h)
+        ok = cudaEventCreateWithFlags(&copied[h], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&freed[h], cudaEventDisableTiming) == cudaSuccess;
+    Workspace ws;
+    if (ok) ok = cudaMemsetAsync(status, 0, sizeof(int32_t), st) == cudaSuccess;
+    if (ok) ok = decode_tables(g, sigma, counts, status, workspace, ws_bytes, st, ws) == SKV_OK;
+    // batch b: copy into half b % 2 once the decode of batch b - 2 is done with it,
+    // then decode it on the compute stream once the copy has landed
+    for (uint64_t b = 0; b < nb && ok; ++b) {
+        const int h = (int)(b & 1u);
+        uint8_t *dst = static_cast<uint8_t *>(staging) + h * half;
+        const uint64_t k0 = first[b], k1 = first[b + 1];
+        const uint64_t o0 = host_offsets[k0], bytes = host_offsets[k1] - o0;
+        if (b >= 2) ok = cudaStreamWaitEvent(cs, freed[h], 0) == cudaSuccess;
+        if (ok) ok = cudaMemcpyAsync(dst, static_cast<const uint8_t *>(host_bitstream) + o0, bytes,
+                                     cudaMemcpyHostToDevice, cs) == cudaSuccess;
+        if (ok) ok = cudaEventRecord(copied[h], cs) == cudaSuccess;
+        if (ok) ok = cudaStreamWaitEvent(st, copied[h], 0) == cudaSuccess;
+        if (ok) {
+            DecArgs da{g, dst, bytes, offsets, static_cast<const uint8_t *>(mu), ws.phat, ws.rsig, ws.qt,
+                       ws.inv_lo, ws.inv_hi, nullptr, k1 - k0, static_cast<uint8_t *>(kv_out),
+                       (uint64_t)g.Tc * g.HD, status, o0, k0};
+            ok = launch_decode(da, st) == 0;
+        }
+        if (ok) ok = cudaEventRecord(freed[h], st) == cudaSuccess;
+    }
+    for (int h = 0; h < 2; ++h) {
+        if (copied[h]) cudaEventDestroy(copied[h]);
+        if (freed[h]) cudaEventDestroy(freed[h]);
+    }
+    std::free(first);
+    return ok ? SKV_OK : SKV_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -31,6 +31,7 @@
 namespace skv {
 
 constexpr int kDecWarps = 8;
+static_assert(kDecWarps * 4 == (int)kDecResidentWarps, "decoder residency");
 constexpr uint32_t kRing = 256;        // words per warp ring
 constexpr uint32_t kBlock = 64;        // words per cp.async batch (16 B per lane, 16 lanes)
 constexpr uint32_t kStepSyms = 4;      // the ring is topped up every 4 symbols
@@ -292,14 +293,15 @@ __global__ void __launch_bounds__(kDecWarps * 32, 4) decode_kernel(const DecArgs
     uint32_t *ring = reinterpret_cast<uint32_t *>(skv_dec_smem + kSmRing) + warp * kRing;
     const uint64_t unit = gid / g.G;
     const uint32_t grp = (uint32_t)(gid % g.G);
-    const uint64_t k = a.ids ? (uint64_t)a.ids[unit] : unit;
+    const uint64_t k = a.ids ? (uint64_t)a.ids[unit] : a.chunk0 + unit;
     if (k >= g.n_chunks) {
         if (lane == 0) set_status(a.status, SKV_ERR_INVALID_ARG);
         return;
     }
     const ChunkSpan cs = chunk_span(g, k);
-    const uint64_t off0 = a.offsets[k], off1 = a.offsets[k + 1];
-    if (off0 > off1 || off1 > a.stream_bytes || (off0 & 15u) || off1 - off0 < g.hdr_bytes) {
+    const uint64_t o0 = a.offsets[k], o1 = a.offsets[k + 1];
+    const uint64_t off0 = o0 - a.origin, off1 = o1 - a.origin;
+    if (o0 < a.origin || o0 > o1 || off1 > a.stream_bytes || (off0 & 15u) || off1 - off0 < g.hdr_bytes) {
         if (lane == 0) set_status(a.status, SKV_ERR_CORRUPT);
         return;
     }

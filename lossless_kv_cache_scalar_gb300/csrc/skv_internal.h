@@ -139,6 +139,9 @@ struct InvArgs {
     uint16_t *inv_hi;      // M entries: max{o : C_hi(o) <= s} (0 if none)
 };
 
+// decode_kernel keeps 4 CTAs of 8 warps resident per SM (its launch bounds).
+constexpr uint32_t kDecResidentWarps = 32;
+
 struct DecArgs {
     Geom g;
     const uint8_t *stream;
@@ -155,6 +158,8 @@ struct DecArgs {
     uint8_t *out;          // canonical layout, or pages of page_elems codes
     uint64_t page_elems;
     int32_t *status;
+    uint64_t origin;       // stream holds the bytes from offset `origin` on (staged decode)
+    uint64_t chunk0;       // without ids: unit u decodes chunk chunk0 + u
 };
 
 struct CdfArgs {
