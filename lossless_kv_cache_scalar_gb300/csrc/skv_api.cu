@@ -223,7 +223,7 @@ static Workspace carve(const Geom &g, int kind, uint8_t *base) {
     o_rsig = off;
     off += round256(4ull * g.n_planes * g.n_sblk * g.HD);
     uint64_t o_ep = 0;
-    if (kind == WS_ENCODE && g.dtype == SKV_BF16) {
+    if ((kind == WS_ENCODE || kind == WS_DECODE_FULL) && g.dtype == SKV_BF16) {
         o_ep = off;
         off += round256(8ull * (d.N + 1));
     }
@@ -256,6 +256,7 @@ static Workspace carve(const Geom &g, int kind, uint8_t *base) {
             w.scratch = reinterpret_cast<uint32_t *>(base + o_scratch);
         } else {
             w.qt = reinterpret_cast<float *>(base + o_qt);
+            if (kind == WS_DECODE_FULL && g.dtype == SKV_BF16) w.ep = reinterpret_cast<uint2 *>(base + o_ep);
             if (kind == WS_DECODE_FULL) {
                 w.inv_lo = reinterpret_cast<uint16_t *>(base + o_lo);
                 w.inv_hi = reinterpret_cast<uint16_t *>(base + o_hi);
@@ -406,7 +407,7 @@ static int32_t decode_launch(const Geom &g, const void *bitstream, uint64_t bits
     DecArgs da{g, static_cast<const uint8_t *>(bitstream), bitstream_bytes, offsets,
                static_cast<const uint8_t *>(mu), ws.phat, ws.rsig, ws.qt, ws.inv_lo, ws.inv_hi,
                pages ? ids : nullptr,
-               n_units, static_cast<uint8_t *>(out), (uint64_t)g.Tc * g.HD, status, 0, 0};
+               n_units, static_cast<uint8_t *>(out), (uint64_t)g.Tc * g.HD, status, 0, 0, ws.ep};
     return launch_decode(da, st) ? SKV_ERR_CUDA : SKV_OK;
 }
 
@@ -630,7 +631,7 @@ int32_t skv_decode_offload(const skv_layout *lay, const void *host_bitstream, ui
         if (ok) {
             DecArgs da{g, dst, bytes, offsets, static_cast<const uint8_t *>(mu), ws.phat, ws.rsig, ws.qt,
                        ws.inv_lo, ws.inv_hi, nullptr, k1 - k0, static_cast<uint8_t *>(kv_out),
-                       (uint64_t)g.Tc * g.HD, status, o0, k0};
+                       (uint64_t)g.Tc * g.HD, status, o0, k0, ws.ep};
             ok = launch_decode(da, st) == 0;
         }
         if (ok) ok = cudaEventRecord(freed[h], st) == cudaSuccess;

@@ -30,8 +30,16 @@
 
 namespace skv {
 
-constexpr int kDecWarps = 8;
-static_assert(kDecWarps * 4 == (int)kDecResidentWarps, "decoder residency");
+// CTA shapes: bf16 runs one CTA of 32 warps per SM (its tables are staged once
+// per SM and the rest of L1 caches the 256 KB P_hat table); e4m3, whose tables
+// all sit in shared memory, runs four CTAs of 8 warps per SM. Both keep 32
+// warps resident.
+template <uint32_t DT> struct DecShape;
+template <> struct DecShape<SKV_BF16> { static constexpr int warps = 32, ctas = 1; };
+template <> struct DecShape<SKV_E4M3> { static constexpr int warps = 8, ctas = 4; };
+static_assert(DecShape<SKV_BF16>::warps * DecShape<SKV_BF16>::ctas == (int)kDecResidentWarps &&
+              DecShape<SKV_E4M3>::warps * DecShape<SKV_E4M3>::ctas == (int)kDecResidentWarps,
+              "decoder residency");
 constexpr uint32_t kRing = 256;        // words per warp ring
 constexpr uint32_t kBlock = 64;        // words per cp.async batch (16 B per lane, 16 lanes)
 constexpr uint32_t kStepSyms = 4;      // the ring is topped up every 4 symbols
@@ -41,7 +49,8 @@ constexpr uint32_t kSmPhi = 0;                                        // Tables
 constexpr uint32_t kSmQt = (sizeof(Tables) + 15u) & ~15u;              // float2[kQuantN + 1]
 constexpr uint32_t kSmT8 = (kSmQt + 8u * (kQuantN + 1) + 15u) & ~15u;  // Tables8
 constexpr uint32_t kSmRing = (kSmT8 + sizeof(Tables8) + 15u) & ~15u;   // uint32 [warps][kRing]
-constexpr uint32_t kDecSmem = kSmRing + kDecWarps * kRing * 4u;
+template <uint32_t DT>
+constexpr uint32_t dec_smem() { return kSmRing + DecShape<DT>::warps * kRing * 4u; }
 
 // ------------------------------------------------------------ search aids
 
@@ -140,6 +149,21 @@ __device__ __forceinline__ const float2 *dqt() {
     return reinterpret_cast<const float2 *>(skv_dec_smem + kSmQt);
 }
 
+// C(o) and P_hat(o) for the decoder: with EP (bf16 and a full workspace) from
+// the per-call (edge bits, P_hat) pair table, else from the code bits and the
+// P_hat table. Both give the same values.
+template <uint32_t DT, bool EP>
+__device__ __forceinline__ uint32_t cdf_dec(const DecArgs &a, uint32_t o, float mu, float rs) {
+    const Weights w{a.g.w_n, a.g.w_w, a.g.w_h};
+    if (EP) return cdf_ep(dtab(), w, a.ep, o, mu, rs);
+    return cdf<DT>(dtab(), dtab8(), w, a.phat, o, mu, rs);
+}
+template <uint32_t DT, bool EP>
+__device__ __forceinline__ uint32_t phat_dec(const DecArgs &a, uint32_t o) {
+    if (EP) return __ldg(&a.ep[o].y);
+    return Codes<DT>::phat(dtab8(), a.phat, o);
+}
+
 // Round a value to the nearest code (ties to even), clamped to the finite codes.
 template <uint32_t DT> __device__ __forceinline__ uint32_t nearest_ord(float x);
 template <> __device__ __forceinline__ uint32_t nearest_ord<SKV_BF16>(float x) {
@@ -186,7 +210,7 @@ __device__ __forceinline__ uint32_t estimate(const DecArgs &a, float kS, float i
 // estimate (1, 2, 4, ... codes), so a near miss ends at once and a far one is
 // bracketed within a factor of two; later rounds split the bracket 33 ways.
 // No 16-bit code space needs more than four rounds after the first.
-template <uint32_t DT>
+template <uint32_t DT, bool EP>
 __device__ __forceinline__ void cooperative_search(const DecArgs &a, uint32_t L, uint32_t s, float mu,
                                                 float rs, uint32_t o, uint32_t clo, uint32_t chi,
                                                 uint32_t &o_out, uint32_t &c_out, uint32_t &f_out) {
@@ -213,7 +237,7 @@ __device__ __forceinline__ void cooperative_search(const DecArgs &a, uint32_t L,
         } else {
             cand = lo + 1u + (uint32_t)(((uint64_t)(span - 1u) * lane) / 32u);
         }
-        const uint32_t c = cdf<DT>(dtab(), dtab8(), w, a.phat, cand, muL, rsL);
+        const uint32_t c = cdf_dec<DT, EP>(a, cand, muL, rsL);
         const uint32_t le = __ballot_sync(0xFFFFFFFFu, c <= sL);   // a prefix of the lanes
         const uint32_t k = __popc(le);
         const uint32_t c_lo = __shfl_sync(0xFFFFFFFFu, c, k ? k - 1u : 0u);
@@ -235,7 +259,7 @@ __device__ __forceinline__ uint32_t saturated_inverse(const DecArgs &a, uint32_t
 
 // The estimated code o for slot s, with c = C(o) and C(o+1) - C(o) in f; the
 // caller checks C(o) <= s < C(o+1) and resolves misses cooperatively.
-template <uint32_t DT>
+template <uint32_t DT, bool EP>
 __device__ __forceinline__ uint32_t find_symbol(const DecArgs &a, float kS, float inv_total,
                                                 uint32_t s, float mu, float rs, uint32_t o_mu,
                                                 uint32_t ph_mu, uint32_t &c_out, uint32_t &f_out) {
@@ -248,14 +272,14 @@ __device__ __forceinline__ uint32_t find_symbol(const DecArgs &a, float kS, floa
         o = estimate<DT>(a, kS, inv_total, s, o_mu, ph_mu, mu, sigma, far, below);
         if (!far) {
             // second pass: p_hat's share and the floor term at the first estimate
-            const uint32_t ph1 = w.h ? K::phat(dtab8(), a.phat, o) : 0u;
+            const uint32_t ph1 = w.h ? phat_dec<DT, EP>(a, o) : 0u;
             o = estimate<DT>(a, kS, inv_total, s, o, ph1, mu, sigma, far, below);
         }
     }
     // only p_hat holds mass this far out: the saturated inverse gives the code
     if (far) o = saturated_inverse<DT>(a, s, (below || !(w.n + w.w)) ? 0u : (w.n + w.w) << 24);
-    const uint32_t clo = cdf<DT>(dtab(), dtab8(), w, a.phat, o, mu, rs);
-    const uint32_t chi = cdf<DT>(dtab(), dtab8(), w, a.phat, o + 1u, mu, rs);
+    const uint32_t clo = cdf_dec<DT, EP>(a, o, mu, rs);
+    const uint32_t chi = cdf_dec<DT, EP>(a, o + 1u, mu, rs);
     c_out = clo;
     f_out = chi - clo;
     return o;
@@ -271,26 +295,17 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
-template <uint32_t DT>
-__global__ void __launch_bounds__(kDecWarps * 32, 4) decode_kernel(const DecArgs a) {
+// Decode one group of 32 streams (gid = chunk unit * G + group) with this warp.
+template <uint32_t DT, bool EP>
+__device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uint32_t *ring) {
     using K = Codes<DT>;
     constexpr uint32_t V = K::V, m = K::m;
     constexpr uint32_t M = 1u << m;
     constexpr uint64_t L = K::L;
     constexpr uint32_t BITS = 8u * K::bytes;
     constexpr uint32_t MASK = (1u << BITS) - 1u;
-    {
-        float *qt = reinterpret_cast<float *>(skv_dec_smem + kSmQt);
-        for (uint32_t i = threadIdx.x; i < kQuantFloats; i += blockDim.x) qt[i] = a.qt[i];
-        stage_tables<DT>(*reinterpret_cast<Tables *>(skv_dec_smem + kSmPhi),
-                         *reinterpret_cast<Tables8 *>(skv_dec_smem + kSmT8), a.phat);
-    }
-
     const Geom &g = a.g;
-    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
-    const uint64_t gid = (uint64_t)blockIdx.x * kDecWarps + warp;
-    if (gid >= a.n_units * g.G) return;
-    uint32_t *ring = reinterpret_cast<uint32_t *>(skv_dec_smem + kSmRing) + warp * kRing;
+    const uint32_t lane = threadIdx.x & 31u;
     const uint64_t unit = gid / g.G;
     const uint32_t grp = (uint32_t)(gid % g.G);
     const uint64_t k = a.ids ? (uint64_t)a.ids[unit] : a.chunk0 + unit;
@@ -361,7 +376,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 4) decode_kernel(const DecArgs
         // per-symbol inputs of the next symbol, loaded one symbol ahead
         uint32_t mc_n = muv.x & MASK;
         float rs_n = active ? __ldg(rse) : 1.0f;
-        uint32_t ph_n = (active && g.w_h) ? K::phat(dtab8(), a.phat, K::ord(K::finite(mc_n) ? mc_n : 0u)) : 0u;
+        uint32_t ph_n = (active && g.w_h) ? phat_dec<DT, EP>(a, K::ord(K::finite(mc_n) ? mc_n : 0u)) : 0u;
         // One symbol per iteration, kept rolled so the loop body stays in the
         // instruction cache; mu codes shift out of the bottom of the vector and
         // decoded codes shift in at the top.
@@ -392,7 +407,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 4) decode_kernel(const DecArgs
             if (e + 1u < V && active) {
                 mc_n = muv.x & MASK;
                 rs_n = __ldg(rse + e + 1u);
-                if (g.w_h) ph_n = K::phat(dtab8(), a.phat, K::ord(K::finite(mc_n) ? mc_n : 0u));
+                if (g.w_h) ph_n = phat_dec<DT, EP>(a, K::ord(K::finite(mc_n) ? mc_n : 0u));
             }
             uint32_t code = 0, slot = 0, o = 0, c = 0, f = 1;
             float mu = 0.0f;
@@ -402,7 +417,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 4) decode_kernel(const DecArgs
                 bad_mu |= !fin;
                 mu = fin ? K::value(mc) : 0.0f;
                 slot = (uint32_t)x & (M - 1u);
-                o = find_symbol<DT>(a, kS, inv_total, slot, mu, rs, K::ord(fin ? mc : 0u), ph, c, f);
+                o = find_symbol<DT, EP>(a, kS, inv_total, slot, mu, rs, K::ord(fin ? mc : 0u), ph, c, f);
                 miss = !(c <= slot && slot - c < f);
             }
             // misses are resolved by the whole warp, one lane at a time
@@ -410,7 +425,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 4) decode_kernel(const DecArgs
             while (pending) {
                 const uint32_t Lm = __ffs(pending) - 1u;
                 pending &= pending - 1u;
-                cooperative_search<DT>(a, Lm, slot, mu, rs, o, c, c + f, o, c, f);
+                cooperative_search<DT, EP>(a, Lm, slot, mu, rs, o, c, c + f, o, c, f);
             }
             if (active) {
                 x = (uint64_t)f * (x >> m) + slot - c;
@@ -442,22 +457,51 @@ __global__ void __launch_bounds__(kDecWarps * 32, 4) decode_kernel(const DecArgs
     if (__any_sync(0xFFFFFFFFu, bad_mu) && lane == 0) set_status(a.status, SKV_ERR_NONFINITE_MU);
 }
 
-int launch_decode(const DecArgs &a, cudaStream_t st) {
-    const uint64_t blocks = (a.n_units * a.g.G + kDecWarps - 1) / kDecWarps;
-    if (blocks == 0) return 0;
-    cudaError_t e;
-    if (a.g.dtype == SKV_BF16) {
-        e = cudaFuncSetAttribute(decode_kernel<SKV_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kDecSmem);
-        if (e != cudaSuccess) return 1;
-        decode_kernel<SKV_BF16><<<(unsigned)blocks, kDecWarps * 32, kDecSmem, st>>>(a);
-    } else {
-        e = cudaFuncSetAttribute(decode_kernel<SKV_E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kDecSmem);
-        if (e != cudaSuccess) return 1;
-        decode_kernel<SKV_E4M3><<<(unsigned)blocks, kDecWarps * 32, kDecSmem, st>>>(a);
+// Each CTA stages the Phi pairs, the quantile table and (e4m3) the code
+// tables, then each warp decodes groups blockIdx.x * warps + warp, then
+// + warps * gridDim.x, ... in turn with its own word ring (bf16: a persistent
+// grid of one CTA per SM; e4m3: one group per warp).
+template <uint32_t DT, bool EP>
+__global__ void __launch_bounds__(DecShape<DT>::warps * 32, DecShape<DT>::ctas) decode_kernel(const DecArgs a) {
+    constexpr int kDecWarps = DecShape<DT>::warps;
+    {
+        float *qt = reinterpret_cast<float *>(skv_dec_smem + kSmQt);
+        for (uint32_t i = threadIdx.x; i < kQuantFloats; i += blockDim.x) qt[i] = a.qt[i];
+        stage_tables<DT>(*reinterpret_cast<Tables *>(skv_dec_smem + kSmPhi),
+                         *reinterpret_cast<Tables8 *>(skv_dec_smem + kSmT8), a.phat);
     }
+    const uint32_t warp = threadIdx.x >> 5;
+    uint32_t *ring = reinterpret_cast<uint32_t *>(skv_dec_smem + kSmRing) + warp * kRing;
+    const uint64_t n_groups = a.n_units * a.g.G;
+    for (uint64_t gid = (uint64_t)blockIdx.x * kDecWarps + warp; gid < n_groups;
+         gid += (uint64_t)gridDim.x * kDecWarps) {
+        decode_group<DT, EP>(a, gid, ring);
+        __syncwarp();
+    }
+}
+
+template <uint32_t DT, bool EP>
+static int launch_decode_t(const DecArgs &a, cudaStream_t st) {
+    constexpr int W = DecShape<DT>::warps;
+    uint64_t blocks = (a.n_units * a.g.G + W - 1) / W;
+    if (blocks == 0) return 0;
+    if (DecShape<DT>::ctas == 1) {             // persistent: at most one CTA per SM
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 1;
+        if (blocks > (uint64_t)sms) blocks = (uint64_t)sms;
+    }
+    if (cudaFuncSetAttribute(decode_kernel<DT, EP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)dec_smem<DT>()) != cudaSuccess)
+        return 1;
+    decode_kernel<DT, EP><<<(unsigned)blocks, W * 32, dec_smem<DT>(), st>>>(a);
     return cudaGetLastError() == cudaSuccess ? 0 : 1;
+}
+
+int launch_decode(const DecArgs &a, cudaStream_t st) {
+    if (a.g.dtype != SKV_BF16) return launch_decode_t<SKV_E4M3, false>(a, st);
+    return a.ep ? launch_decode_t<SKV_BF16, true>(a, st) : launch_decode_t<SKV_BF16, false>(a, st);
 }
 
 }  // namespace skv

@@ -160,6 +160,7 @@ struct DecArgs {
     int32_t *status;
     uint64_t origin;       // stream holds the bytes from offset `origin` on (staged decode)
     uint64_t chunk0;       // without ids: unit u decodes chunk chunk0 + u
+    const uint2 *ep;       // bf16 (edge bits, P_hat) pairs, or NULL: built from the code bits
 };
 
 struct CdfArgs {
