@@ -202,6 +202,7 @@ struct Workspace {
     float *qt;
     uint16_t *inv_lo, *inv_hi;
     uint64_t *states;
+    unsigned long long *ctr;
     uint32_t *nwords;
     uint32_t *scratch;
     uint64_t bytes;
@@ -227,7 +228,10 @@ static Workspace carve(const Geom &g, int kind, uint8_t *base) {
         o_ep = off;
         off += round256(8ull * (d.N + 1));
     }
+    uint64_t o_ctr = 0;
     if (kind == WS_ENCODE) {
+        o_ctr = off;
+        off += 256;
         o_states = off;
         off += round256(8ull * 32ull * g.n_groups);
         o_nwords = off;
@@ -252,6 +256,7 @@ static Workspace carve(const Geom &g, int kind, uint8_t *base) {
         if (kind == WS_ENCODE) {
             if (g.dtype == SKV_BF16) w.ep = reinterpret_cast<uint2 *>(base + o_ep);
             w.states = reinterpret_cast<uint64_t *>(base + o_states);
+            w.ctr = reinterpret_cast<unsigned long long *>(base + o_ctr);
             w.nwords = reinterpret_cast<uint32_t *>(base + o_nwords);
             w.scratch = reinterpret_cast<uint32_t *>(base + o_scratch);
         } else {
@@ -376,7 +381,8 @@ int32_t skv_encode(const skv_layout *lay, const void *kv, const void *mu, const 
     const Workspace ws = carve(g, WS_ENCODE, static_cast<uint8_t *>(workspace));
     if ((r = run_setup(g, sigma, counts, ws, status, st)) != SKV_OK) return r;
     EncArgs ea{g, static_cast<const uint8_t *>(kv), static_cast<const uint8_t *>(mu), ws.phat,
-               ws.ep, ws.rsig, ws.states, ws.nwords, ws.scratch, status};
+               ws.ep, ws.rsig, ws.states, ws.nwords, ws.scratch, status, ws.ctr};
+    if (cudaMemsetAsync(ws.ctr, 0, sizeof(unsigned long long), st) != cudaSuccess) return SKV_ERR_CUDA;
     if (launch_encode(ea, st)) return SKV_ERR_CUDA;
     ScanArgs sa{g, ws.nwords, offsets, out_capacity, status};
     if (launch_scan(sa, st)) return SKV_ERR_CUDA;

@@ -15,7 +15,12 @@
 
 namespace skv {
 
-constexpr int kEncWarps = 8;
+// Warps of the one persistent CTA per SM: bf16 runs 32 (64 registers each;
+// more warps in flight hide the serial rANS chain better than more registers
+// per warp), e4m3, with twice the scalars per vector, 16.
+template <uint32_t DT> struct EncShape;
+template <> struct EncShape<SKV_BF16> { static constexpr int warps = 32; };
+template <> struct EncShape<SKV_E4M3> { static constexpr int warps = 16; };
 
 // Model phase for scalars [e0, e0 + 8) of a vector: (c, f) and 1/f of each.
 // No branches and no dependence on the rANS state, so the eight evaluations
@@ -49,18 +54,14 @@ __device__ __forceinline__ void model8(const Tables &tab, const Tables8 &tab8, c
     }
 }
 
+// Encode one group of 32 streams (gid = chunk * G + group) with this warp.
 template <uint32_t DT>
-__global__ void __launch_bounds__(kEncWarps * 32, 3) encode_kernel(const EncArgs a) {
+__device__ __forceinline__ void encode_group(const EncArgs &a, const Tables &tab, const Tables8 &tab8,
+                                             uint64_t gid) {
     using K = Codes<DT>;
     constexpr uint32_t V = K::V;
-    __shared__ Tables tab;
-    __shared__ Tables8 tab8;
-    stage_tables<DT>(tab, tab8, a.phat);
-
     const Geom &g = a.g;
-    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
-    const uint64_t gid = (uint64_t)blockIdx.x * kEncWarps + warp;
-    if (gid >= g.n_groups) return;
+    const uint32_t lane = threadIdx.x & 31u;
     const uint64_t k = gid / g.G;
     const uint32_t grp = (uint32_t)(gid % g.G);
     const ChunkSpan cs = chunk_span(g, k);
@@ -136,6 +137,25 @@ __global__ void __launch_bounds__(kEncWarps * 32, 3) encode_kernel(const EncArgs
     if (__any_sync(0xFFFFFFFFu, overflow) && lane == 0) set_status(a.status, SKV_ERR_CAPACITY);
 }
 
+// One persistent CTA per SM: the tables are staged once, then each warp takes
+// the next group from a global counter until none are left, so warps stay
+// busy until the end and no CTA waits on its slowest warp.
+template <uint32_t DT>
+__global__ void __launch_bounds__(EncShape<DT>::warps * 32, 1) encode_kernel(const EncArgs a) {
+    __shared__ Tables tab;
+    __shared__ Tables8 tab8;
+    stage_tables<DT>(tab, tab8, a.phat);
+    const uint32_t lane = threadIdx.x & 31u;
+    for (;;) {
+        unsigned long long gid = 0;
+        if (lane == 0) gid = atomicAdd(a.next_group, 1ull);
+        gid = __shfl_sync(0xFFFFFFFFu, gid, 0);
+        if (gid >= a.g.n_groups) break;
+        encode_group<DT>(a, tab, tab8, gid);
+        __syncwarp();
+    }
+}
+
 // Per-chunk sizes (FORMAT.md section 7) and their exclusive scan into offsets.
 __global__ void __launch_bounds__(1024) scan_kernel(const ScanArgs a) {
     const Geom &g = a.g;
@@ -207,14 +227,22 @@ __global__ void __launch_bounds__(256) compact_kernel(const CompactArgs a) {
     }
 }
 
-int launch_encode(const EncArgs &a, cudaStream_t st) {
-    const uint64_t blocks = (a.g.n_groups + kEncWarps - 1) / kEncWarps;
+template <uint32_t DT>
+static int launch_encode_t(const EncArgs &a, cudaStream_t st) {
+    constexpr int W = EncShape<DT>::warps;
+    uint64_t blocks = (a.g.n_groups + W - 1) / W;
     if (blocks == 0) return 0;
-    if (a.g.dtype == SKV_BF16)
-        encode_kernel<SKV_BF16><<<(unsigned)blocks, kEncWarps * 32, 0, st>>>(a);
-    else
-        encode_kernel<SKV_E4M3><<<(unsigned)blocks, kEncWarps * 32, 0, st>>>(a);
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 1;
+    if (blocks > (uint64_t)sms) blocks = (uint64_t)sms;
+    encode_kernel<DT><<<(unsigned)blocks, W * 32, 0, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? 0 : 1;
+}
+
+int launch_encode(const EncArgs &a, cudaStream_t st) {
+    return a.g.dtype == SKV_BF16 ? launch_encode_t<SKV_BF16>(a, st) : launch_encode_t<SKV_E4M3>(a, st);
 }
 
 int launch_scan(const ScanArgs &a, cudaStream_t st) {

@@ -99,6 +99,7 @@ struct EncArgs {
     uint32_t *nwords;      // n_groups
     uint32_t *scratch;     // n_groups * cap_words
     int32_t *status;
+    unsigned long long *next_group;   // work counter, 0 at launch
 };
 
 struct ScanArgs {
