@@ -458,9 +458,10 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
 }
 
 // Each CTA stages the Phi pairs, the quantile table and (e4m3) the code
-// tables, then each warp decodes groups blockIdx.x * warps + warp, then
-// + warps * gridDim.x, ... in turn with its own word ring (bf16: a persistent
-// grid of one CTA per SM; e4m3: one group per warp).
+// tables, then each warp decodes groups warp * gridDim.x + blockIdx.x, then
+// + warps * gridDim.x, ... in turn with its own word ring (consecutive groups
+// go to different CTAs, so a few pages spread over many SMs). bf16: a
+// persistent grid of at most one CTA per SM; e4m3: one group per warp.
 template <uint32_t DT, bool EP>
 __global__ void __launch_bounds__(DecShape<DT>::warps * 32, DecShape<DT>::ctas) decode_kernel(const DecArgs a) {
     constexpr int kDecWarps = DecShape<DT>::warps;
@@ -473,7 +474,7 @@ __global__ void __launch_bounds__(DecShape<DT>::warps * 32, DecShape<DT>::ctas) 
     const uint32_t warp = threadIdx.x >> 5;
     uint32_t *ring = reinterpret_cast<uint32_t *>(skv_dec_smem + kSmRing) + warp * kRing;
     const uint64_t n_groups = a.n_units * a.g.G;
-    for (uint64_t gid = (uint64_t)blockIdx.x * kDecWarps + warp; gid < n_groups;
+    for (uint64_t gid = (uint64_t)warp * gridDim.x + blockIdx.x; gid < n_groups;
          gid += (uint64_t)gridDim.x * kDecWarps) {
         decode_group<DT, EP>(a, gid, ring);
         __syncwarp();
@@ -483,9 +484,11 @@ __global__ void __launch_bounds__(DecShape<DT>::warps * 32, DecShape<DT>::ctas) 
 template <uint32_t DT, bool EP>
 static int launch_decode_t(const DecArgs &a, cudaStream_t st) {
     constexpr int W = DecShape<DT>::warps;
-    uint64_t blocks = (a.n_units * a.g.G + W - 1) / W;
+    const uint64_t n_groups = a.n_units * a.g.G;
+    uint64_t blocks = (n_groups + W - 1) / W;
     if (blocks == 0) return 0;
-    if (DecShape<DT>::ctas == 1) {             // persistent: at most one CTA per SM
+    if (DecShape<DT>::ctas == 1) {             // persistent: one CTA per SM, at least one group each
+        blocks = n_groups;
         int dev = 0, sms = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)

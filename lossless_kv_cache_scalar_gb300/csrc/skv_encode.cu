@@ -137,22 +137,25 @@ __device__ __forceinline__ void encode_group(const EncArgs &a, const Tables &tab
     if (__any_sync(0xFFFFFFFFu, overflow) && lane == 0) set_status(a.status, SKV_ERR_CAPACITY);
 }
 
-// One persistent CTA per SM: the tables are staged once, then each warp takes
-// the next group from a global counter until none are left, so warps stay
-// busy until the end and no CTA waits on its slowest warp.
+// One persistent CTA per SM: the tables are staged once; each warp's first
+// group is warp * gridDim.x + blockIdx.x (so a small input spreads over all
+// SMs instead of filling the first CTAs), and after that each warp takes the
+// next group from a global counter until none are left, so warps stay busy
+// until the end and no CTA waits on its slowest warp.
 template <uint32_t DT>
 __global__ void __launch_bounds__(EncShape<DT>::warps * 32, 1) encode_kernel(const EncArgs a) {
     __shared__ Tables tab;
     __shared__ Tables8 tab8;
     stage_tables<DT>(tab, tab8, a.phat);
-    const uint32_t lane = threadIdx.x & 31u;
-    for (;;) {
-        unsigned long long gid = 0;
-        if (lane == 0) gid = atomicAdd(a.next_group, 1ull);
-        gid = __shfl_sync(0xFFFFFFFFu, gid, 0);
-        if (gid >= a.g.n_groups) break;
+    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+    const uint64_t first_dynamic = (uint64_t)gridDim.x * EncShape<DT>::warps;
+    uint64_t gid = (uint64_t)warp * gridDim.x + blockIdx.x;
+    while (gid < a.g.n_groups) {
         encode_group<DT>(a, tab, tab8, gid);
         __syncwarp();
+        unsigned long long t = 0;
+        if (lane == 0) t = atomicAdd(a.next_group, 1ull);
+        gid = first_dynamic + __shfl_sync(0xFFFFFFFFu, t, 0);
     }
 }
 
@@ -230,7 +233,7 @@ __global__ void __launch_bounds__(256) compact_kernel(const CompactArgs a) {
 template <uint32_t DT>
 static int launch_encode_t(const EncArgs &a, cudaStream_t st) {
     constexpr int W = EncShape<DT>::warps;
-    uint64_t blocks = (a.g.n_groups + W - 1) / W;
+    uint64_t blocks = a.g.n_groups;            // at most one CTA per SM, at least one group each
     if (blocks == 0) return 0;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
