@@ -175,6 +175,8 @@ def main():
     ap.add_argument("--offload", type=int, default=1,
                     help="time the offload decode from pinned host memory (0: skip)")
     ap.add_argument("--staging-mb", type=int, default=1024, help="offload staging buffer (two halves)")
+    ap.add_argument("--requant", type=int, default=1,
+                    help="time skv_requantize (8 -> 4 bits) on the workload's KV quantised to 8 bits (0: skip)")
     ap.add_argument("--model-inputs", type=int, default=1,
                     help="time skv_histogram and skv_calibrate_sigma on the workload (0: skip)")
     ap.add_argument("--traffic-json", default=os.path.join(ROOT, "profiles", "traffic.json"))
@@ -272,6 +274,7 @@ def main():
     page_lat = page_latency(coder, out, offsets, w, lay, args, dev) if args.page_latency else None
     inputs = model_inputs_run(w, lay, args, dev, hbm_peak) if args.model_inputs else None
     offload = offload_run(coder, out, offsets, w, lay, args, dev, total_bytes) if args.offload else None
+    requant = requant_run(w, lay, dev, hbm_peak) if (args.requant and lay.dtype == "bf16") else None
     bits = 8.0 * total_bytes / n_el
 
     # end to end through the public API with host buffers
@@ -316,6 +319,7 @@ def main():
             "page_decode_latency_us": page_lat,
             "model_inputs": inputs,
             "offload": offload,
+            "requantize": requant,
             "e2e": e2e,
             "gpu_launches": 8 * args.steps,
             "clocks": clocks,
@@ -459,6 +463,54 @@ def offload_run(coder, out, offsets, w, lay, args, dev, total_bytes, reps=3):
             "staging_mb": args.staging_mb, "batches": n_batches,
             "note": "GB/s of uncompressed KV for decode; link = pinned host-to-device copy of the "
                     "compressed stream / of the raw KV; median of %d" % reps}
+
+
+def requant_run(w, lay, dev, hbm_peak, reps=5, group=128):
+    """The PM-KVQ step beside the coder: KV values quantised to 8 bits (min/max
+    per token and 128 channels; torch, input preparation only), then lowered
+    to 4 bits by skv_requantize with each of the page's three rules. The values
+    are the workload's predictor codes mu, which have the cache's shape and
+    per-channel scales but none of its 2% uniform-random outlier codes (those
+    span the whole bf16 range and defeat any 8-bit min/max grid).
+    Device time of the ERS call (median of `reps`, CUDA events), and the RMS
+    reconstruction error of each rule against the 8-bit values."""
+    from lossless_kv_cache_scalar_gb300.api import requantize
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        v = w["mu"].view(torch.bfloat16).reshape(-1, group)
+        lo = v.min(1).values.float()
+        scale = ((v.max(1).values.float() - lo) / 255.0).clamp_min(1e-30)
+        q = torch.empty(v.numel(), dtype=torch.uint8, device=dev)
+        rows = 1 << 22
+        for r0 in range(0, v.shape[0], rows):           # in slices, to bound the temporaries
+            vr = v[r0:r0 + rows].float()
+            q.view(-1, group)[r0:r0 + rows] = torch.round((vr - lo[r0:r0 + rows, None])
+                                                          / scale[r0:r0 + rows, None]).clamp(0, 255).to(torch.uint8)
+        ts = []
+        for i in range(3 + reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            out, s_out = requantize(q, q.numel(), 4, scale, group, "ers", stream=stream)
+            e1.record(stream)
+            stream.synchronize()
+            if i >= 3:
+                ts.append(e0.elapsed_time(e1))
+        t = float(np.median(ts))
+        err = {}
+        rs = min(v.shape[0], (1 << 26) // group)          # rows in the error sample
+        x8 = lo[:rs, None] + scale[:rs, None] * q.view(-1, group)[:rs].float()
+        for mode in ("ers", "drs", "mrs"):
+            o4, s4 = requantize(q, q.numel(), 4, scale, group, mode, stream=stream)
+            nib = torch.stack([o4[: rs * group // 2] & 15, o4[: rs * group // 2] >> 4], 1).reshape(rs, group).float()
+            x4 = lo[:rs, None] + s4[:rs, None] * nib
+            err[mode] = float(torch.sqrt(torch.mean((x4 - x8) ** 2)) / torch.sqrt(torch.mean(x8 ** 2)))
+        stream.synchronize()
+    nbytes = q.numel() + q.numel() // 2
+    return {"bits": "8 -> 4", "mode": "ers", "ms": t, "gbs": nbytes / t / 1e6, "hbm_frac": nbytes / t / 1e6 / hbm_peak,
+            "codes": q.numel(), "group": group,
+            "relative_rms_error_vs_8bit": err,
+            "values": "the workload's mu codes (bf16), 8-bit min/max per 128 channels",
+            "note": "HBM-bound: reads the 8-bit codes, writes 4-bit codes; error over the first 2^26 codes"}
 
 
 def offload_plan_host(host_offs, batch_bytes, max_chunks):

@@ -316,6 +316,29 @@ int32_t skv_calibrate_sigma(const skv_layout *lay, const void *kv, const void *m
                             uint64_t t_cal, float *sigma, void *stream);
 
 /*
+ * Lower quantised KV codes from 2b to b bits (the progressive quantisation of
+ * PM-KVQ, which the third page's PM-KVQ section describes next to the coder;
+ * a lossy step outside the lossless path). mode:
+ *   SKV_RQ_ERS  Equivalent Right Shift: zero point kept, scale_out = fl32((2^b + 1)
+ *               scale_in), code round(q / (2^b + 1)) -- the same as dequantising
+ *               with scale_in and requantising with scale_out, done with integer
+ *               adds and shifts;
+ *   SKV_RQ_DRS  Direct Right Shift: q >> b, scale_out = 2^b scale_in;
+ *   SKV_RQ_MRS  Modified Right Shift (round instead of truncate):
+ *               min((q + 2^(b-1)) >> b, 2^b - 1), scale_out = 2^b scale_in.
+ *  b           1, 2, 4 or 8 (2 -> 1, 4 -> 2, 8 -> 4, 16 -> 8 bits)
+ *  in          device, n codes of 2b bits packed from the least significant bit
+ *              (code i in bits [2b i, 2b i + 2b) of the byte string), 16-byte aligned
+ *  out         device, n b / 8 bytes of b-bit codes packed the same way, 16-byte aligned
+ *  n           a multiple of 8 / b
+ *  scale_in, scale_out  device float32, one per group of `group` consecutive codes
+ * No device errors.
+ */
+enum { SKV_RQ_ERS = 0, SKV_RQ_DRS = 1, SKV_RQ_MRS = 2 };
+int32_t skv_requantize(uint32_t mode, uint32_t b, const void *in, uint64_t n, void *out,
+                       const float *scale_in, float *scale_out, uint64_t group, void *stream);
+
+/*
  * Decode without any caller-provided scratch (the pages describe no such
  * call; it serves deployment only). Same contract and outputs as skv_decode,
  * minus the workspace arguments. It is meant for callers that cannot call

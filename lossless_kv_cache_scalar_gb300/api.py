@@ -363,3 +363,25 @@ def offload_plan(host_offsets, batch_bytes: int, max_chunks: int = 0) -> list:
                                                          out.ctypes.data_as(C.c_void_p), out.size,
                                                          C.byref(nb)))
     return [int(v) for v in out]
+
+
+RQ_MODES = {"ers": 0, "drs": 1, "mrs": 2}
+
+
+def requantize(codes: torch.Tensor, n: int, b: int, scale: torch.Tensor, group: int, mode: str = "ers",
+               stream=None):
+    """skv_requantize: packed 2b-bit codes (uint8 CUDA tensor) -> (packed b-bit codes,
+    new scales). mode "ers" (Equivalent Right Shift), "drs" or "mrs"."""
+    if not codes.is_cuda or codes.dtype != torch.uint8 or not codes.is_contiguous():
+        raise ValueError("codes must be a contiguous uint8 CUDA tensor")
+    if codes.numel() * 8 < n * 2 * b:
+        raise ValueError("codes holds fewer than n codes of 2b bits")
+    n_groups = -(-n // group)
+    if scale.dtype != torch.float32 or not scale.is_cuda or scale.numel() < n_groups:
+        raise ValueError("scale must be a float32 CUDA tensor with one entry per group")
+    out = torch.empty(max(n * b // 8, 16), dtype=torch.uint8, device=codes.device)
+    s_out = torch.empty(max(n_groups, 1), dtype=torch.float32, device=codes.device)
+    rc = B.lib().skv_requantize(RQ_MODES[mode], b, _ptr(codes), n, _ptr(out), _ptr(scale), _ptr(s_out), group,
+                                _stream_handle(stream))
+    B.check("skv_requantize", rc)
+    return out[: n * b // 8], s_out[:n_groups]

@@ -19,6 +19,8 @@ int launch_histogram(uint32_t dtype, const void *codes, uint64_t n, unsigned lon
                      cudaStream_t st);
 int launch_calibrate(const Geom &g, const void *kv, const void *mu, const uint8_t *mask,
                      uint64_t t_cal, float *sigma, cudaStream_t st);
+int launch_requantize(uint32_t mode, uint32_t b, const void *in, uint64_t n, void *out, const float *s_in,
+                      float *s_out, uint64_t n_groups, cudaStream_t st);
 int launch_search_aids(const Geom &g, const uint32_t *phat, float *qt, uint16_t *inv_lo,
                        uint16_t *inv_hi, cudaStream_t st);
 
@@ -648,6 +650,19 @@ int32_t skv_decode_offload(const skv_layout *lay, const void *host_bitstream, ui
     }
     std::free(first);
     return ok ? SKV_OK : SKV_ERR_CUDA;
+}
+
+int32_t skv_requantize(uint32_t mode, uint32_t b, const void *in, uint64_t n, void *out,
+                       const float *scale_in, float *scale_out, uint64_t group, void *stream) {
+    if (mode > SKV_RQ_MRS || !(b == 1 || b == 2 || b == 4 || b == 8) || group == 0) return SKV_ERR_INVALID_ARG;
+    if ((n * b) % 8 != 0) return SKV_ERR_INVALID_ARG;
+    if (n == 0) return SKV_OK;
+    if (!in || !out || !aligned16(in) || !aligned16(out) || !scale_in || !scale_out ||
+        ((uintptr_t)scale_in & 3u) || ((uintptr_t)scale_out & 3u))
+        return SKV_ERR_INVALID_ARG;
+    const uint64_t n_groups = (n + group - 1) / group;
+    return launch_requantize(mode, b, in, n, out, scale_in, scale_out, n_groups,
+                             static_cast<cudaStream_t>(stream)) ? SKV_ERR_CUDA : SKV_OK;
 }
 
 }  // extern "C"

@@ -118,6 +118,7 @@ def lib():
         L.oracle_model_bits.argtypes = [C.POINTER(_Layout), vp, vp, vp, vp]
         L.oracle_histogram.argtypes = [u32, vp, u64, vp, C.c_int]
         L.oracle_calibrate_sigma.argtypes = [C.POINTER(_Layout), vp, vp, vp, u64, vp]
+        L.oracle_requantize.argtypes = [u32, u32, vp, u64, vp, vp, vp, vp, u64]
         _lib = L
     return _lib
 
@@ -306,3 +307,25 @@ def calibrate_sigma(lay: Layout, kv: np.ndarray, mu: np.ndarray, t_cal: int,
     _check(lib().oracle_calibrate_sigma(C.byref(lay.c()), _p(kv), _p(mu), _p(mask), int(t_cal),
                                         _p(out)))
     return out
+
+
+# ------------------------------------- context page: 2b-bit -> b-bit codes
+
+RQ_ERS, RQ_DRS, RQ_MRS = 0, 1, 2
+
+
+def requantize(mode: int, b: int, packed_in: np.ndarray, n: int, scale_in, group: int, zero_in=None):
+    """(packed b-bit codes uint8[n b / 8], new scales float32[n_groups]) from
+    packed 2b-bit codes (PM-KVQ section: ERS / DRS / MRS)."""
+    packed_in = np.ascontiguousarray(packed_in, np.uint8).reshape(-1)
+    scale_in = np.ascontiguousarray(scale_in, np.float32).reshape(-1)
+    n_groups = -(-n // group)
+    if packed_in.size * 8 < n * 2 * b or scale_in.size < n_groups:
+        raise ValueError("inputs shorter than n codes / n_groups scales")
+    if zero_in is not None:
+        zero_in = np.ascontiguousarray(zero_in, np.float32).reshape(-1)
+    out = np.zeros(max(n * b // 8, 1), np.uint8)
+    sc = np.zeros(max(n_groups, 1), np.float32)
+    _check(lib().oracle_requantize(mode, b, _p(packed_in), n, _p(out), _p(scale_in), _p(zero_in),
+                                   _p(sc), group))
+    return out[: n * b // 8], sc[:n_groups]

@@ -934,3 +934,56 @@ int oracle_calibrate_sigma(const or_layout *lay, const void *kv, const void *mu,
     }
     return OR_OK;
 }
+
+/* ------------------- context page: requantising 2b-bit codes to b bits */
+
+/*
+ * The PM-KVQ section of the third page (progressive quantisation of the KV
+ * cache, 16 -> 8 -> 4 -> 2 bits) lowers a 2b-bit code to b bits. Its
+ * Equivalent Right Shift keeps the zero point and sets the new scale to
+ * S_b = (2^b + 1) S_2b, which the page shows equals dequantising and
+ * requantising; written here as exactly that: x = z + S_2b q (binary64),
+ * q_b = round((x - z) / S_b). The two shift baselines the page's ablation
+ * names are written as plain shifts: Direct Right Shift q >> b, and (this
+ * build's reading of "rounding-corrected") Modified Right Shift
+ * min((q + 2^(b-1)) >> b, 2^b - 1); both imply the scale 2^b S_2b.
+ * Codes are packed LSB first (code i in bits [w i, w i + w) of the byte
+ * string, w = 2b on input, b on output); one scale (and zero) per `group`
+ * consecutive codes. mode: 0 ERS, 1 DRS, 2 MRS.
+ */
+int oracle_requantize(uint32_t mode, uint32_t b, const uint8_t *in, uint64_t n, uint8_t *out,
+                      const float *scale_in, const float *zero_in, float *scale_out, uint64_t group)
+{
+    if (mode > 2 || !(b == 1 || b == 2 || b == 4 || b == 8) || group == 0) return OR_ERR_INVALID_ARG;
+    if ((n * b) % 8 != 0 || (n && (!in || !out || !scale_in || !scale_out))) return OR_ERR_INVALID_ARG;
+    const uint32_t w = 2 * b;
+    uint64_t n_groups = (n + group - 1) / group;
+    if (mode == 0)          /* dequantising needs finite, positive scales */
+        for (uint64_t g = 0; g < n_groups; ++g)
+            if (!(scale_in[g] > 0.0f && scale_in[g] <= 0x1.fffffep127f)) return OR_ERR_INVALID_ARG;
+    memset(out, 0, n * b / 8);
+    for (uint64_t i = 0; i < n; ++i) {
+        uint64_t bit = i * w;
+        uint32_t q = 0;
+        for (uint32_t k = 0; k < w; ++k) q |= (uint32_t)((in[(bit + k) / 8] >> ((bit + k) % 8)) & 1u) << k;
+        uint64_t g = i / group;
+        uint32_t r;
+        if (mode == 0) {
+            double S2 = scale_in[g], z = zero_in ? zero_in[g] : 0.0;
+            double Sb = (double)((1u << b) + 1u) * S2;
+            double x = z + S2 * (double)q;
+            r = (uint32_t)floor((x - z) / Sb + 0.5);
+        } else if (mode == 1) {
+            r = q >> b;
+        } else {
+            r = (q + (1u << (b - 1))) >> b;
+            if (r > (1u << b) - 1u) r = (1u << b) - 1u;
+        }
+        uint64_t ob = i * b;
+        for (uint32_t k = 0; k < b; ++k) out[(ob + k) / 8] |= (uint8_t)(((r >> k) & 1u) << ((ob + k) % 8));
+    }
+    for (uint64_t g = 0; g < n_groups; ++g)
+        scale_out[g] = mode == 0 ? (float)((double)((1u << b) + 1u) * (double)scale_in[g])
+                                 : (float)((double)(1u << b) * (double)scale_in[g]);
+    return OR_OK;
+}
