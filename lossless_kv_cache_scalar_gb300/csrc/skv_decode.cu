@@ -17,7 +17,7 @@
 // (w_n + w_w); a table in t = -log2(min(g, 1 - g)) gives z = G^-1(g); and
 // mu + z sigma rounded to the code grid is the estimate (a code owns the reals
 // that round to it, FORMAT.md section 2). A first pass takes the reference at
-// mu's own code, a second at the first estimate. A far outlier that only
+// mu's own code, a second (bf16) at the first estimate. A far outlier that only
 // p_hat explains (both Gaussians saturated, so C is a mu-independent function
 // of o) is read from per-call inverse tables instead. When the test fails,
 // the whole warp searches for that lane's code together (cooperative_search).
@@ -188,11 +188,11 @@ __device__ __forceinline__ uint32_t estimate(const DecArgs &a, float kS, float i
     constexpr int MN = (int)((1u << K::m) - K::N);
     const float ph = (float)(a.g.w_h * ph_ref);
     const float ph_top = (float)(a.g.w_h << 24) - ph;
+    // the quantile of the Gaussian part, measured from whichever end is nearer
     const int d = (int)s - (int)o_ref;
-    const float g_lo = fmaxf(fmaf((float)max(d, 0), kS, -ph) * inv_total, 0.0f);
-    const float g_hi = fmaxf(fmaf((float)max(MN - d, 0), kS, -ph_top) * inv_total, 0.0f);
-    below = g_lo <= g_hi;
-    const float gt = fminf(g_lo, g_hi);
+    below = fmaf((float)d, kS, -ph) * inv_total <= 0.5f;
+    const int dd = below ? max(d, 0) : max(MN - d, 0);
+    const float gt = fmaxf(fmaf((float)dd, kS, below ? -ph : -ph_top) * inv_total, 0.0f);
     far = gt < 9.094947e-13f;                       // 2^-40
     const float u = fminf(fmaxf(fmaf(-__log2f(gt), (float)kQuantSteps, -(float)kQuantSteps), 0.0f),
                           (float)kQuantN - 0.001f);
@@ -270,8 +270,10 @@ __device__ __forceinline__ uint32_t find_symbol(const DecArgs &a, float kS, floa
     if (w.n + w.w) {
         const float sigma = __fdividef(1.0f, rs);
         o = estimate<DT>(a, kS, inv_total, s, o_mu, ph_mu, mu, sigma, far, below);
-        if (!far) {
+        if (DT == SKV_BF16 && !far) {
             // second pass: p_hat's share and the floor term at the first estimate
+            // (bf16 only: e4m3's eight codes per binade leave the first estimate
+            // as good as a second one, which measured 14% slower there)
             const uint32_t ph1 = w.h ? phat_dec<DT, EP>(a, o) : 0u;
             o = estimate<DT>(a, kS, inv_total, s, o, ph1, mu, sigma, far, below);
         }
@@ -377,10 +379,10 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
         uint32_t mc_n = muv.x & MASK;
         float rs_n = active ? __ldg(rse) : 1.0f;
         uint32_t ph_n = (active && g.w_h) ? phat_dec<DT, EP>(a, K::ord(K::finite(mc_n) ? mc_n : 0u)) : 0u;
-        // One symbol per iteration, kept rolled so the loop body stays in the
-        // instruction cache; mu codes shift out of the bottom of the vector and
-        // decoded codes shift in at the top.
-#pragma unroll 1
+        // One symbol per iteration, unrolled only twice so the loop body stays
+        // in the instruction cache; mu codes shift out of the bottom of the
+        // vector and decoded codes shift in at the top.
+#pragma unroll 2
         for (uint32_t e = 0; e < V; ++e) {
             if ((e & (kStepSyms - 1u)) == 0u) {
                 // Keep the ring ahead of the reader: 4 symbols use at most 128 words.
