@@ -177,6 +177,8 @@ def main():
     ap.add_argument("--staging-mb", type=int, default=1024, help="offload staging buffer (two halves)")
     ap.add_argument("--requant", type=int, default=1,
                     help="time skv_requantize (8 -> 4 bits) on the workload's KV quantised to 8 bits (0: skip)")
+    ap.add_argument("--alu-probe", type=int, default=1,
+                    help="measure the integer / binary32 issue rates with skv_peak_probe (0: skip)")
     ap.add_argument("--model-inputs", type=int, default=1,
                     help="time skv_histogram and skv_calibrate_sigma on the workload (0: skip)")
     ap.add_argument("--traffic-json", default=os.path.join(ROOT, "profiles", "traffic.json"))
@@ -271,6 +273,7 @@ def main():
     except (OSError, ValueError):
         traffic = None
     hbm_peak = _peaks().get("hbm_gbs", 6685.5)
+    measured_peaks = alu_peaks(dev) if args.alu_probe else None
     page_lat = page_latency(coder, out, offsets, w, lay, args, dev) if args.page_latency else None
     inputs = model_inputs_run(w, lay, args, dev, hbm_peak) if args.model_inputs else None
     offload = offload_run(coder, out, offsets, w, lay, args, dev, total_bytes) if args.offload else None
@@ -312,6 +315,8 @@ def main():
                          "alg_ops_per_scalar": ALG_OPS[(lay.dtype, dom)],
                          "peak_basis": f"{SMS} SMs x {LANES_PER_SM_CLK} lane-ops/clk x {sm_mhz:.0f} MHz (sampled)",
                          "hbm_bound_gbs": hbm_peak * lay.bytes_per_code / (2 * lay.bytes_per_code + bits / 8),
+                         "measured_issue_tops": measured_peaks,
+                         "frac_of_measured_mix": (achieved / measured_peaks["mix"]) if measured_peaks else None,
                          "hbm_peak_gbs": hbm_peak},
             "roofline_encode_frac": ALG_OPS[(lay.dtype, "encode")] * n_el / (t_enc / args.steps) / 1e12 / peak_tops,
             "roofline_decode_frac": ALG_OPS[(lay.dtype, "decode")] * n_el / (t_dec / args.steps) / 1e12 / peak_tops,
@@ -511,6 +516,43 @@ def requant_run(w, lay, dev, hbm_peak, reps=5, group=128):
             "relative_rms_error_vs_8bit": err,
             "values": "the workload's mu codes (bf16), 8-bit min/max per 128 channels",
             "note": "HBM-bound: reads the 8-bit codes, writes 4-bit codes; error over the first 2^26 codes"}
+
+
+def alu_peaks(dev, target_ms=20.0):
+    """Issue-rate probes (skv_peak_probe): 32-bit Tops/s for three-input
+    integer add, lop3, integer multiply-add, binary32 multiply and their 1:1:1:1
+    mix, each the best of 3 launches sized to about target_ms."""
+    import ctypes as C
+    from lossless_kv_cache_scalar_gb300 import _binding as B
+    stream = torch.cuda.Stream(device=dev)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    names = ["iadd3", "lop3", "imad", "fmul", "mix"]
+    out = {}
+    for kind, name in enumerate(names):
+        iters = 64
+        for _ in range(8):                       # grow until a launch takes target_ms
+            ops = C.c_uint64()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            B.check("skv_peak_probe", B.lib().skv_peak_probe(kind, iters, C.c_void_p(sink.data_ptr()),
+                                                             C.byref(ops), C.c_void_p(stream.cuda_stream)))
+            e1.record(stream)
+            stream.synchronize()
+            ms = e0.elapsed_time(e1)
+            if ms >= target_ms / 2 or iters >= (1 << 20):
+                break
+            iters = int(iters * max(2.0, target_ms / max(ms, 1e-3)))
+        best = 0.0
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            B.check("skv_peak_probe", B.lib().skv_peak_probe(kind, iters, C.c_void_p(sink.data_ptr()),
+                                                             C.byref(ops), C.c_void_p(stream.cuda_stream)))
+            e1.record(stream)
+            stream.synchronize()
+            best = max(best, ops.value / (e0.elapsed_time(e1) / 1e3) / 1e12)
+        out[name] = best
+    return out
 
 
 def offload_plan_host(host_offs, batch_bytes, max_chunks):

@@ -339,6 +339,18 @@ int32_t skv_requantize(uint32_t mode, uint32_t b, const void *in, uint64_t n, vo
                        const float *scale_in, float *scale_out, uint64_t group, void *stream);
 
 /*
+ * Measurement aid (the pages describe no such call): one launch of an
+ * arithmetic issue-rate probe, for the arithmetic roofline of the coder's
+ * kernels. kind: 0 three-input integer add, 1 three-input logic (lop3),
+ * 2 integer multiply-add, 3 binary32 multiply, 4 the four in turn. Every SM
+ * runs 8 CTAs of 256 threads, each thread 8 independent chains for
+ * iters x 16 steps. *ops receives the 32-bit operations the launch issues
+ * (host, at once); time the launch on `stream` (CUDA events) to get the rate.
+ * sink: device uint32, written only if the chains hit one unlikely value.
+ */
+int32_t skv_peak_probe(int32_t kind, uint32_t iters, uint32_t *sink, uint64_t *ops, void *stream);
+
+/*
  * Decode without any caller-provided scratch (the pages describe no such
  * call; it serves deployment only). Same contract and outputs as skv_decode,
  * minus the workspace arguments. It is meant for callers that cannot call

@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libskv.so")
 BUILD = os.path.join(os.path.dirname(HERE), "_build")
-SOURCES = ["skv_api.cu", "skv_encode.cu", "skv_decode.cu", "skv_calib.cu", "skv_rq.cu", "skv_noalloc.cu"]
+SOURCES = ["skv_api.cu", "skv_encode.cu", "skv_decode.cu", "skv_calib.cu", "skv_rq.cu", "skv_peak.cu", "skv_noalloc.cu"]
 HEADERS = ["skv_model.cuh", "skv_internal.h", "phi_q24.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-ftz=false", "-prec-div=true",

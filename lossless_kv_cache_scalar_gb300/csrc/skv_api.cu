@@ -21,6 +21,8 @@ int launch_calibrate(const Geom &g, const void *kv, const void *mu, const uint8_
                      uint64_t t_cal, float *sigma, cudaStream_t st);
 int launch_requantize(uint32_t mode, uint32_t b, const void *in, uint64_t n, void *out, const float *s_in,
                       float *s_out, uint64_t n_groups, cudaStream_t st);
+int launch_peak(int kind, uint32_t iters, uint32_t *sink, uint32_t blocks, cudaStream_t st);
+uint64_t peak_ops(int kind, uint32_t iters, uint32_t blocks);
 int launch_search_aids(const Geom &g, const uint32_t *phat, float *qt, uint16_t *inv_lo,
                        uint16_t *inv_hi, cudaStream_t st);
 
@@ -663,6 +665,17 @@ int32_t skv_requantize(uint32_t mode, uint32_t b, const void *in, uint64_t n, vo
     const uint64_t n_groups = (n + group - 1) / group;
     return launch_requantize(mode, b, in, n, out, scale_in, scale_out, n_groups,
                              static_cast<cudaStream_t>(stream)) ? SKV_ERR_CUDA : SKV_OK;
+}
+
+int32_t skv_peak_probe(int32_t kind, uint32_t iters, uint32_t *sink, uint64_t *ops, void *stream) {
+    if (kind < 0 || kind > 4 || iters == 0 || !sink || !ops) return SKV_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return SKV_ERR_CUDA;
+    const uint32_t blocks = (uint32_t)sms * 8u;
+    *ops = peak_ops(kind, iters, blocks);
+    return launch_peak(kind, iters, sink, blocks, static_cast<cudaStream_t>(stream)) ? SKV_ERR_CUDA : SKV_OK;
 }
 
 }  // extern "C"
