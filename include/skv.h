@@ -316,6 +316,39 @@ int32_t skv_calibrate_sigma(const skv_layout *lay, const void *kv, const void *m
                             uint64_t t_cal, float *sigma, void *stream);
 
 /*
+ * Encode and decode with the cache in host memory (the offload use of the
+ * wiki's uses section, end to end): batches of layers_per_batch layers go
+ * through two halves of a device staging buffer, host-to-device copies on
+ * copy_stream and device-to-host copies on copy_out_stream overlapping each
+ * other and the kernels on stream (three distinct streams). The
+ * bitstream is byte for byte skv_encode's (chunks code independently, and a
+ * batch is a run of whole chunks). Both calls return when everything has
+ * landed in host memory; host buffers should be page-locked for the copies to
+ * overlap. Device errors go to *status as in skv_encode / skv_decode.
+ *  skv_host_staging_bytes  device staging both calls need: op 1 encode, 0 decode,
+ *                          2 decode with the outlier inverse tables (faster);
+ *                          decode uses them whenever staging_bytes allows
+ *  skv_encode_host  host_kv, host_mu: codes in canonical layout (host);
+ *                   host_out: out_capacity bytes (host); host_offsets: uint64[n_chunks + 1]
+ *                   (host, written); returns SKV_ERR_CAPACITY if the stream does not fit
+ *  skv_decode_host  host_bits / host_offsets as skv_encode_host wrote them; host_kv_out
+ *                   (host, canonical layout); offsets that descend, pass bitstream_bytes or
+ *                   give a batch more bytes than its half holds return SKV_ERR_CORRUPT
+ * sigma and counts are device arrays as for skv_encode.
+ */
+int32_t skv_host_staging_bytes(const skv_layout *lay, uint32_t layers_per_batch, int32_t op,
+                               uint64_t *bytes);
+int32_t skv_encode_host(const skv_layout *lay, const void *host_kv, const void *host_mu, const float *sigma,
+                        const uint64_t *counts, void *host_out, uint64_t out_capacity,
+                        uint64_t *host_offsets, int32_t *status, void *staging, uint64_t staging_bytes,
+                        uint32_t layers_per_batch, void *stream, void *copy_stream, void *copy_out_stream);
+int32_t skv_decode_host(const skv_layout *lay, const void *host_bits, uint64_t bitstream_bytes,
+                        const uint64_t *host_offsets, const void *host_mu, const float *sigma,
+                        const uint64_t *counts, void *host_kv_out, int32_t *status, void *staging,
+                        uint64_t staging_bytes, uint32_t layers_per_batch, void *stream, void *copy_stream,
+                        void *copy_out_stream);
+
+/*
  * Lower quantised KV codes from 2b to b bits (the progressive quantisation of
  * PM-KVQ, which the third page's PM-KVQ section describes next to the coder;
  * a lossy step outside the lossless path). mode:

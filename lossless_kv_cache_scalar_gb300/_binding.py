@@ -50,6 +50,9 @@ SIGNATURES = {
     "skv_decode_offload": (_i32, [_LP, _vp, _u64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _u64, _vp,
                                   _u64, _vp, _vp]),
     "skv_requantize": (_i32, [_u32, _u32, _vp, _u64, _vp, _vp, _vp, _u64, _vp]),
+    "skv_host_staging_bytes": (_i32, [_LP, _u32, _i32, C.POINTER(_u64)]),
+    "skv_encode_host": (_i32, [_LP, _vp, _vp, _vp, _vp, _vp, _u64, _vp, _vp, _vp, _u64, _u32, _vp, _vp, _vp]),
+    "skv_decode_host": (_i32, [_LP, _vp, _u64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _u64, _u32, _vp, _vp, _vp]),
     "skv_peak_probe": (_i32, [_i32, _u32, _vp, C.POINTER(_u64), _vp]),
     "skv_offload_plan": (_i32, [_vp, _u64, _u64, _u64, _vp, _u64, C.POINTER(_u64)]),
     "skv_calibrate_sigma": (_i32, [_LP, _vp, _vp, _vp, _u64, _vp, _vp]),

@@ -385,3 +385,75 @@ def requantize(codes: torch.Tensor, n: int, b: int, scale: torch.Tensor, group: 
                                 _stream_handle(stream))
     B.check("skv_requantize", rc)
     return out[: n * b // 8], s_out[:n_groups]
+
+
+class HostCoder:
+    """skv_encode_host / skv_decode_host: the cache and the bitstream live in
+    (page-locked) host memory; batches of `layers_per_batch` layers stream
+    through a device staging buffer with copies overlapping the kernels."""
+
+    def __init__(self, layout: Layout, device="cuda", layers_per_batch: int | None = None,
+                 fast_decode: bool = True):
+        """layers_per_batch None: four batches (each fills most of the GPU on
+        caches of Qwen3-8B size, and copies of three of them overlap compute)."""
+        self.layout = layout
+        self.device = torch.device(device)
+        self.lpb = int(layers_per_batch) if layers_per_batch else max(1, -(-layout.n_layers // 4))
+        self._c = layout.c()
+        need = 0
+        for op in (1, 2 if fast_decode else 0):
+            v = C.c_uint64()
+            B.check("skv_host_staging_bytes", B.lib().skv_host_staging_bytes(C.byref(self._c), self.lpb, op, C.byref(v)))
+            need = max(need, v.value)
+        self.staging = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.copy_stream = torch.cuda.Stream(device=self.device)       # host to device
+        self.copy_out_stream = torch.cuda.Stream(device=self.device)   # device to host
+        self.n_chunks = layout.n_chunks
+
+    def _check_host(self, t, what, nbytes=None):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{what} must be a contiguous CPU tensor (page-locked for overlap)")
+        if nbytes is not None and t.numel() * t.element_size() < nbytes:
+            raise ValueError(f"{what} is smaller than {nbytes} bytes")
+
+    def check_status(self, where):
+        torch.cuda.synchronize(self.device)
+        st = int(self.status.item())
+        if st:
+            raise B.SKVError(where, st)
+
+    def encode_into(self, kv, mu, sigma, counts, out, offsets, stream=None):
+        """kv, mu: host codes (canonical layout); out: host uint8 buffer; offsets: host
+        int64 [n_chunks + 1] (written). Returns the stream's byte count."""
+        lay = self.layout
+        raw = lay.n_elems * lay.bytes_per_code
+        self._check_host(kv, "kv", raw)
+        self._check_host(mu, "mu", raw)
+        self._check_host(out, "out")
+        self._check_host(offsets, "offsets", 8 * (self.n_chunks + 1))
+        _check_model_inputs(lay, sigma, counts)
+        rc = B.lib().skv_encode_host(C.byref(self._c), C.c_void_p(kv.data_ptr()), C.c_void_p(mu.data_ptr()),
+                                     _ptr(sigma), _ptr(counts), C.c_void_p(out.data_ptr()),
+                                     out.numel() * out.element_size(), C.c_void_p(offsets.data_ptr()),
+                                     _ptr(self.status), _ptr(self.staging), self.staging.numel(), self.lpb,
+                                     _stream_handle(stream), C.c_void_p(self.copy_stream.cuda_stream),
+                                     C.c_void_p(self.copy_out_stream.cuda_stream))
+        B.check("skv_encode_host", rc)
+        return int(offsets[-1])
+
+    def decode_into(self, bits, nbytes, offsets, mu, sigma, counts, kv_out, stream=None):
+        lay = self.layout
+        raw = lay.n_elems * lay.bytes_per_code
+        self._check_host(bits, "bits", nbytes)
+        self._check_host(offsets, "offsets", 8 * (self.n_chunks + 1))
+        self._check_host(mu, "mu", raw)
+        self._check_host(kv_out, "kv_out", raw)
+        _check_model_inputs(lay, sigma, counts)
+        rc = B.lib().skv_decode_host(C.byref(self._c), C.c_void_p(bits.data_ptr()), nbytes,
+                                     C.c_void_p(offsets.data_ptr()), C.c_void_p(mu.data_ptr()), _ptr(sigma),
+                                     _ptr(counts), C.c_void_p(kv_out.data_ptr()), _ptr(self.status),
+                                     _ptr(self.staging), self.staging.numel(), self.lpb, _stream_handle(stream),
+                                     C.c_void_p(self.copy_stream.cuda_stream),
+                                     C.c_void_p(self.copy_out_stream.cuda_stream))
+        B.check("skv_decode_host", rc)

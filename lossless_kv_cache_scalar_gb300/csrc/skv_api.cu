@@ -295,6 +295,119 @@ static int32_t common_checks(const Geom &g, const float *sigma, const uint64_t *
     return SKV_OK;
 }
 
+// ------------------------------------------------ host-buffer pipelines
+
+// A sub-layout of layers [l0, l0 + nl) of lay: its chunks are chunks
+// [2 l0 P, 2 (l0 + nl) P) of the whole cache (planes are layer-major), and its
+// bitstream is the same bytes as theirs (chunks code independently).
+static skv_layout sub_layout(const skv_layout *lay, uint32_t nl) {
+    skv_layout s = *lay;
+    s.n_layers = nl;
+    return s;
+}
+
+// Device staging of the host pipelines for batches of `lpb` layers: the
+// decoder's or encoder's tables for the whole layout, then two halves.
+struct HostStaging {
+    uint32_t *phat;
+    float *rsig;
+    uint2 *ep;             // bf16 (edge, P_hat) pairs (encode; decode with inverse tables)
+    float *qt;             // decode
+    uint16_t *inv_lo, *inv_hi;
+    uint64_t *states;      // encode: one batch
+    unsigned long long *ctr;
+    uint32_t *nwords;
+    uint32_t *scratch;
+    uint8_t *kv[2], *mu[2], *bits[2];
+    uint64_t *offs[2];
+    uint64_t out_cap;      // bytes of bits[h]
+    uint64_t bytes;
+};
+
+static HostStaging carve_host(const Geom &g, const Geom &gb, bool encode, bool inv, uint8_t *base) {
+    const DtypeInfo d = dtype_info(g.dtype);
+    uint64_t off = 0;
+    auto take = [&](uint64_t n) { const uint64_t o = off; off += round256(n); return o; };
+    const uint64_t o_phat = take(4ull * (d.N + 1));
+    const uint64_t o_rsig = take(4ull * g.n_planes * g.n_sblk * g.HD);
+    const bool ep = g.dtype == SKV_BF16 && (encode || inv);
+    const uint64_t o_ep = ep ? take(8ull * (d.N + 1)) : 0;
+    uint64_t o_qt = 0, o_lo = 0, o_hi = 0, o_states = 0, o_ctr = 0, o_nw = 0, o_scr = 0;
+    if (encode) {
+        o_states = take(8ull * 32ull * gb.n_groups);
+        o_ctr = take(8);
+        o_nw = take(4ull * gb.n_groups);
+        o_scr = take(4ull * gb.cap_words * gb.n_groups);
+    } else {
+        o_qt = take(4ull * kQuantFloats);
+        if (inv) { o_lo = take(2ull << d.m); o_hi = take(2ull << d.m); }
+    }
+    const uint64_t raw = gb.n_planes * gb.T * gb.HD * d.bytes;
+    uint64_t cap = 0;
+    {
+        const uint64_t full = chunk_max_bytes(gb, (uint64_t)gb.Tc * gb.HD / d.V);
+        const uint64_t last = chunk_max_bytes(gb, (gb.T - (gb.P - 1) * gb.Tc) * gb.HD / d.V);
+        cap = gb.n_chunks ? gb.n_planes * ((gb.P - 1) * full + last) : 0;
+    }
+    uint64_t o_kv[2], o_mu[2], o_bits[2], o_offs[2];
+    for (int h = 0; h < 2; ++h) {
+        o_kv[h] = take(raw);
+        o_mu[h] = take(raw);
+        o_bits[h] = take(cap);
+        o_offs[h] = take(8ull * (gb.n_chunks + 1));
+    }
+    HostStaging st{};
+    st.bytes = off;
+    st.out_cap = cap;
+    if (base) {
+        st.phat = reinterpret_cast<uint32_t *>(base + o_phat);
+        st.rsig = reinterpret_cast<float *>(base + o_rsig);
+        if (ep) st.ep = reinterpret_cast<uint2 *>(base + o_ep);
+        if (encode) {
+            st.states = reinterpret_cast<uint64_t *>(base + o_states);
+            st.ctr = reinterpret_cast<unsigned long long *>(base + o_ctr);
+            st.nwords = reinterpret_cast<uint32_t *>(base + o_nw);
+            st.scratch = reinterpret_cast<uint32_t *>(base + o_scr);
+        } else {
+            st.qt = reinterpret_cast<float *>(base + o_qt);
+            if (inv) {
+                st.inv_lo = reinterpret_cast<uint16_t *>(base + o_lo);
+                st.inv_hi = reinterpret_cast<uint16_t *>(base + o_hi);
+            }
+        }
+        for (int h = 0; h < 2; ++h) {
+            st.kv[h] = base + o_kv[h];
+            st.mu[h] = base + o_mu[h];
+            st.bits[h] = base + o_bits[h];
+            st.offs[h] = reinterpret_cast<uint64_t *>(base + o_offs[h]);
+        }
+    }
+    return st;
+}
+
+// Geometry of the batch layout (lpb layers), checked.
+static int32_t batch_geom(const skv_layout *lay, uint32_t lpb, Geom &g, Geom &gb) {
+    int32_t r = make_geom(lay, g);
+    if (r != SKV_OK) return r;
+    if (lpb == 0) return SKV_ERR_INVALID_ARG;
+    if (lpb > lay->n_layers) lpb = lay->n_layers;
+    const skv_layout sb = sub_layout(lay, lpb);
+    return make_geom(&sb, gb);
+}
+
+struct EventPair {
+    cudaEvent_t e[2] = {nullptr, nullptr};
+    bool make() {
+        for (int h = 0; h < 2; ++h)
+            if (cudaEventCreateWithFlags(&e[h], cudaEventDisableTiming) != cudaSuccess) return false;
+        return true;
+    }
+    ~EventPair() {
+        for (int h = 0; h < 2; ++h)
+            if (e[h]) cudaEventDestroy(e[h]);
+    }
+};
+
 }  // namespace skv
 
 using namespace skv;
@@ -676,6 +789,195 @@ int32_t skv_peak_probe(int32_t kind, uint32_t iters, uint32_t *sink, uint64_t *o
     const uint32_t blocks = (uint32_t)sms * 8u;
     *ops = peak_ops(kind, iters, blocks);
     return launch_peak(kind, iters, sink, blocks, static_cast<cudaStream_t>(stream)) ? SKV_ERR_CUDA : SKV_OK;
+}
+
+int32_t skv_host_staging_bytes(const skv_layout *lay, uint32_t layers_per_batch, int32_t op,
+                               uint64_t *bytes) {
+    Geom g, gb;
+    if (!bytes || (op != 0 && op != 1 && op != 2)) return SKV_ERR_INVALID_ARG;
+    const int32_t r = batch_geom(lay, layers_per_batch, g, gb);
+    if (r != SKV_OK) return r;
+    *bytes = carve_host(g, gb, op == 1, op == 2, nullptr).bytes;
+    return SKV_OK;
+}
+
+int32_t skv_encode_host(const skv_layout *lay, const void *host_kv, const void *host_mu, const float *sigma,
+                        const uint64_t *counts, void *host_out, uint64_t out_capacity,
+                        uint64_t *host_offsets, int32_t *status, void *staging, uint64_t staging_bytes,
+                        uint32_t layers_per_batch, void *stream, void *copy_stream, void *copy_out_stream) {
+    Geom g, gb;
+    int32_t r = batch_geom(lay, layers_per_batch, g, gb);
+    if (r != SKV_OK) return r;
+    const uint32_t lpb = layers_per_batch < lay->n_layers ? layers_per_batch : lay->n_layers;
+    if (!sigma || !status || (g.w_h && !counts) || !host_offsets) return SKV_ERR_INVALID_ARG;
+    if (g.n_chunks && (!host_kv || !host_mu || !host_out)) return SKV_ERR_INVALID_ARG;
+    if (!staging || ((uintptr_t)staging & 255u) || staging_bytes < carve_host(g, gb, true, false, nullptr).bytes)
+        return SKV_ERR_INVALID_ARG;
+    const HostStaging hs = carve_host(g, gb, true, false, static_cast<uint8_t *>(staging));
+    cudaStream_t st = static_cast<cudaStream_t>(stream), cs = static_cast<cudaStream_t>(copy_stream);
+    cudaStream_t os = static_cast<cudaStream_t>(copy_out_stream);
+    EventPair copied, encoded, drained;
+    if (!copied.make() || !encoded.make() || !drained.make()) return SKV_ERR_CUDA;
+    if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return SKV_ERR_CUDA;
+    host_offsets[0] = 0;
+    if (g.n_chunks == 0) return SKV_OK;
+    // tables for the whole cache, once (P_hat, 1/sigma, bf16 pairs)
+    SetupArgs sa{g, sigma, counts, hs.phat, hs.rsig, hs.ep, status};
+    {
+        const uint64_t nsig = g.n_planes * g.n_sblk * g.HD;
+        const unsigned grid = (unsigned)(1 + (nsig > 65536 ? (nsig - 65536 + 65535) / 65536 : 0));
+        if (g.dtype == SKV_BF16) setup_kernel<SKV_BF16><<<grid < 1024 ? grid : 1024, 1024, 0, st>>>(sa);
+        else setup_kernel<SKV_E4M3><<<grid < 1024 ? grid : 1024, 1024, 0, st>>>(sa);
+        if (cudaGetLastError() != cudaSuccess) return SKV_ERR_CUDA;
+    }
+    const DtypeInfo d = dtype_info(g.dtype);
+    const uint64_t plane_elems = g.T * g.HD;
+    const uint32_t nb = (lay->n_layers + lpb - 1) / lpb;
+    uint64_t base = 0;
+    int32_t rc = SKV_OK;
+    // batch b: copy in (copy stream), encode, scan, compact (stream), copy out
+    // (copy-out stream, so copies in and out run at once); its output is
+    // collected once the next batch is queued, so the host's wait for the
+    // batch's size overlaps the GPU's work on the next one
+    auto collect = [&](uint32_t b) -> int32_t {
+        const int h = (int)(b & 1u);
+        const uint32_t l0 = b * lpb, nl = lay->n_layers - l0 < lpb ? lay->n_layers - l0 : lpb;
+        const skv_layout sl = sub_layout(lay, nl);
+        Geom gs;
+        make_geom(&sl, gs);
+        const uint64_t kk0 = (uint64_t)l0 * lay->n_kv * g.P;      // the batch's first chunk
+        if (cudaStreamWaitEvent(os, encoded.e[h], 0) != cudaSuccess) return SKV_ERR_CUDA;
+        if (cudaMemcpyAsync(host_offsets + kk0, hs.offs[h], 8ull * (gs.n_chunks + 1), cudaMemcpyDeviceToHost,
+                            os) != cudaSuccess || cudaStreamSynchronize(os) != cudaSuccess)
+            return SKV_ERR_CUDA;
+        const uint64_t total = host_offsets[kk0 + gs.n_chunks];
+        if (total > hs.out_cap || base + total > out_capacity) return SKV_ERR_CAPACITY;
+        for (uint64_t j = 0; j <= gs.n_chunks; ++j) host_offsets[kk0 + j] += base;
+        if (total && cudaMemcpyAsync(static_cast<uint8_t *>(host_out) + base, hs.bits[h], total,
+                                     cudaMemcpyDeviceToHost, os) != cudaSuccess)
+            return SKV_ERR_CUDA;
+        if (cudaEventRecord(drained.e[h], os) != cudaSuccess) return SKV_ERR_CUDA;
+        base += total;
+        return SKV_OK;
+    };
+    for (uint32_t b = 0; b < nb && rc == SKV_OK; ++b) {
+        const int h = (int)(b & 1u);
+        const uint32_t l0 = b * lpb, nl = lay->n_layers - l0 < lpb ? lay->n_layers - l0 : lpb;
+        const skv_layout sl = sub_layout(lay, nl);
+        Geom gs;
+        make_geom(&sl, gs);
+        const uint64_t e0 = (uint64_t)l0 * lay->n_kv * plane_elems, ne = (uint64_t)nl * lay->n_kv * plane_elems;
+        // half h is free once batch b - 2 has been encoded (inputs) and copied out (output)
+        if ((b >= 2 && cudaStreamWaitEvent(cs, encoded.e[h], 0) != cudaSuccess) ||
+            cudaMemcpyAsync(hs.kv[h], static_cast<const uint8_t *>(host_kv) + e0 * d.bytes, ne * d.bytes,
+                            cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+            cudaMemcpyAsync(hs.mu[h], static_cast<const uint8_t *>(host_mu) + e0 * d.bytes, ne * d.bytes,
+                            cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+            cudaEventRecord(copied.e[h], cs) != cudaSuccess || cudaStreamWaitEvent(st, copied.e[h], 0) != cudaSuccess ||
+            (b >= 2 && cudaStreamWaitEvent(st, drained.e[h], 0) != cudaSuccess) ||
+            cudaMemsetAsync(hs.ctr, 0, sizeof(unsigned long long), st) != cudaSuccess) {
+            rc = SKV_ERR_CUDA;
+            break;
+        }
+        EncArgs ea{gs, hs.kv[h], hs.mu[h], hs.phat, hs.ep, hs.rsig + (uint64_t)l0 * lay->n_kv * g.n_sblk * g.HD,
+                   hs.states, hs.nwords, hs.scratch, status, hs.ctr};
+        ScanArgs sc{gs, hs.nwords, hs.offs[h], hs.out_cap, status};
+        CompactArgs ca{gs, hs.states, hs.nwords, hs.scratch, hs.offs[h], hs.bits[h], hs.out_cap};
+        if (launch_encode(ea, st) || launch_scan(sc, st) || launch_compact(ca, st) ||
+            cudaEventRecord(encoded.e[h], st) != cudaSuccess) {
+            rc = SKV_ERR_CUDA;
+            break;
+        }
+        if (b >= 1) rc = collect(b - 1);
+    }
+    if (rc == SKV_OK) rc = collect(nb - 1);
+    // nothing of this call may still be running when it returns (the staging
+    // is reused by the next call), whichever way it ends
+    const bool done = cudaStreamSynchronize(cs) == cudaSuccess && cudaStreamSynchronize(st) == cudaSuccess &&
+                      cudaStreamSynchronize(os) == cudaSuccess;
+    return rc != SKV_OK ? rc : (done ? SKV_OK : SKV_ERR_CUDA);
+}
+
+int32_t skv_decode_host(const skv_layout *lay, const void *host_bits, uint64_t bitstream_bytes,
+                        const uint64_t *host_offsets, const void *host_mu, const float *sigma,
+                        const uint64_t *counts, void *host_kv_out, int32_t *status, void *staging,
+                        uint64_t staging_bytes, uint32_t layers_per_batch, void *stream, void *copy_stream,
+                        void *copy_out_stream) {
+    Geom g, gb;
+    int32_t r = batch_geom(lay, layers_per_batch, g, gb);
+    if (r != SKV_OK) return r;
+    const uint32_t lpb = layers_per_batch < lay->n_layers ? layers_per_batch : lay->n_layers;
+    if (!sigma || !status || (g.w_h && !counts) || !host_offsets) return SKV_ERR_INVALID_ARG;
+    if (g.n_chunks && (!host_bits || !host_mu || !host_kv_out)) return SKV_ERR_INVALID_ARG;
+    const bool inv = staging_bytes >= carve_host(g, gb, false, true, nullptr).bytes;
+    if (!staging || ((uintptr_t)staging & 255u) || staging_bytes < carve_host(g, gb, false, false, nullptr).bytes)
+        return SKV_ERR_INVALID_ARG;
+    if (g.n_chunks && host_offsets[0] != 0) return SKV_ERR_CORRUPT;
+    for (uint64_t k = 0; k < g.n_chunks; ++k)
+        if (host_offsets[k + 1] < host_offsets[k]) return SKV_ERR_CORRUPT;
+    if (g.n_chunks && host_offsets[g.n_chunks] > bitstream_bytes) return SKV_ERR_CORRUPT;
+    const HostStaging hs = carve_host(g, gb, false, inv, static_cast<uint8_t *>(staging));
+    // a batch's bytes must fit its half
+    const uint32_t nb = (lay->n_layers + lpb - 1) / lpb;
+    for (uint32_t b = 0; b < nb; ++b) {
+        const uint64_t k0 = (uint64_t)b * lpb * lay->n_kv * g.P;
+        const uint64_t k1 = std::min<uint64_t>(g.n_chunks, k0 + (uint64_t)lpb * lay->n_kv * g.P);
+        if (host_offsets[k1] - host_offsets[k0] > hs.out_cap) return SKV_ERR_CORRUPT;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream), cs = static_cast<cudaStream_t>(copy_stream);
+    cudaStream_t os = static_cast<cudaStream_t>(copy_out_stream);
+    EventPair copied, decoded, drained;
+    if (!copied.make() || !decoded.make() || !drained.make()) return SKV_ERR_CUDA;
+    if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return SKV_ERR_CUDA;
+    if (g.n_chunks == 0) return SKV_OK;
+    Workspace ws{};
+    ws.phat = hs.phat; ws.rsig = hs.rsig; ws.qt = hs.qt; ws.inv_lo = hs.inv_lo; ws.inv_hi = hs.inv_hi; ws.ep = hs.ep;
+    {
+        SetupArgs sa{g, sigma, counts, ws.phat, ws.rsig, ws.ep, status};
+        const uint64_t nsig = g.n_planes * g.n_sblk * g.HD;
+        const unsigned grid = (unsigned)(1 + (nsig > 65536 ? (nsig - 65536 + 65535) / 65536 : 0));
+        if (g.dtype == SKV_BF16) setup_kernel<SKV_BF16><<<grid < 1024 ? grid : 1024, 1024, 0, st>>>(sa);
+        else setup_kernel<SKV_E4M3><<<grid < 1024 ? grid : 1024, 1024, 0, st>>>(sa);
+        if (cudaGetLastError() != cudaSuccess) return SKV_ERR_CUDA;
+        if (launch_search_aids(g, ws.phat, ws.qt, ws.inv_lo, ws.inv_hi, st)) return SKV_ERR_CUDA;
+    }
+    const DtypeInfo d = dtype_info(g.dtype);
+    const uint64_t plane_elems = g.T * g.HD;
+    int32_t rc = SKV_OK;
+    for (uint32_t b = 0; b < nb; ++b) {
+        const int h = (int)(b & 1u);
+        const uint32_t l0 = b * lpb, nl = lay->n_layers - l0 < lpb ? lay->n_layers - l0 : lpb;
+        const skv_layout sl = sub_layout(lay, nl);
+        Geom gs;
+        make_geom(&sl, gs);
+        const uint64_t k0 = (uint64_t)l0 * lay->n_kv * g.P;
+        const uint64_t o0 = host_offsets[k0], nbytes = host_offsets[k0 + gs.n_chunks] - o0;
+        const uint64_t e0 = (uint64_t)l0 * lay->n_kv * plane_elems, ne = (uint64_t)nl * lay->n_kv * plane_elems;
+        // half h is free once batch b - 2 has been decoded (inputs) and drained (output)
+        bool ok = (b < 2 || cudaStreamWaitEvent(cs, decoded.e[h], 0) == cudaSuccess);
+        ok = ok && cudaMemcpyAsync(hs.offs[h], host_offsets + k0, 8ull * (gs.n_chunks + 1), cudaMemcpyHostToDevice,
+                                   cs) == cudaSuccess;
+        ok = ok && (!nbytes || cudaMemcpyAsync(hs.bits[h], static_cast<const uint8_t *>(host_bits) + o0, nbytes,
+                                               cudaMemcpyHostToDevice, cs) == cudaSuccess);
+        ok = ok && cudaMemcpyAsync(hs.mu[h], static_cast<const uint8_t *>(host_mu) + e0 * d.bytes, ne * d.bytes,
+                                   cudaMemcpyHostToDevice, cs) == cudaSuccess;
+        ok = ok && cudaEventRecord(copied.e[h], cs) == cudaSuccess;
+        ok = ok && cudaStreamWaitEvent(st, copied.e[h], 0) == cudaSuccess;
+        ok = ok && (b < 2 || cudaStreamWaitEvent(st, drained.e[h], 0) == cudaSuccess);
+        if (!ok) { rc = SKV_ERR_CUDA; break; }
+        DecArgs da{gs, hs.bits[h], nbytes, hs.offs[h], hs.mu[h], ws.phat,
+                   ws.rsig + (uint64_t)l0 * lay->n_kv * g.n_sblk * g.HD, ws.qt, ws.inv_lo, ws.inv_hi, nullptr,
+                   gs.n_chunks, hs.kv[h], (uint64_t)g.Tc * g.HD, status, o0, 0, ws.ep};
+        if (launch_decode(da, st) || cudaEventRecord(decoded.e[h], st) != cudaSuccess) { rc = SKV_ERR_CUDA; break; }
+        ok = cudaStreamWaitEvent(os, decoded.e[h], 0) == cudaSuccess;
+        ok = ok && cudaMemcpyAsync(static_cast<uint8_t *>(host_kv_out) + e0 * d.bytes, hs.kv[h], ne * d.bytes,
+                                   cudaMemcpyDeviceToHost, os) == cudaSuccess;
+        ok = ok && cudaEventRecord(drained.e[h], os) == cudaSuccess;
+        if (!ok) { rc = SKV_ERR_CUDA; break; }
+    }
+    const bool drained_all = cudaStreamSynchronize(cs) == cudaSuccess && cudaStreamSynchronize(st) == cudaSuccess &&
+                             cudaStreamSynchronize(os) == cudaSuccess;
+    return rc != SKV_OK ? rc : (drained_all ? SKV_OK : SKV_ERR_CUDA);
 }
 
 }  // extern "C"
