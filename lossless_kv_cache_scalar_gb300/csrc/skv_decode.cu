@@ -365,15 +365,14 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
     uint32_t rp = 0;        // next word to consume (warp-uniform)
     uint32_t filled = 0;    // words requested into the ring so far (warp-uniform)
 
-    uint4 mu_n = make_uint4(0, 0, 0, 0);
-    if (0 < nq) mu_n = __ldg(reinterpret_cast<const uint4 *>(mup) + s);
 
     for (int64_t j = 0; j < nq0; ++j) {
         const bool active = j < nq;
         const uint64_t q = s + (uint64_t)j * g.W;
         const float *rse = rsp + (uint32_t)((q * V) % g.HD);
-        uint4 muv = mu_n;
-        if (j + 1 < nq) mu_n = __ldg(reinterpret_cast<const uint4 *>(mup) + q + g.W);
+        // mu of this vector (not prefetched: the registers are worth more than
+        // the latency, which the other 31 warps hide)
+        uint4 muv = active ? __ldg(reinterpret_cast<const uint4 *>(mup) + q) : make_uint4(0, 0, 0, 0);
         uint4 outv = make_uint4(0, 0, 0, 0);
         // per-symbol inputs of the next symbol, loaded one symbol ahead
         uint32_t mc_n = muv.x & MASK;
