@@ -582,15 +582,22 @@ def e2e_run(coder, w, lay, args, dev, total_bytes):
     back_h = torch.empty(kv_h.shape, dtype=kv_h.dtype).pin_memory()
     stream = torch.cuda.Stream(device=dev)
     steps = max(1, min(args.steps, 3))
+    t_enc, t_dec = [], []
     with torch.cuda.stream(stream):
         for i in range(1 + steps):
             if i == 1:
                 torch.cuda.synchronize(dev)
                 t0 = time.perf_counter()
+            ta = time.perf_counter()
             sig_d.copy_(sig_h, non_blocking=True)
             cnt_d.copy_(cnt_h, non_blocking=True)
             n = hc.encode_into(kv_h, mu_h, sig_d, cnt_d, out_h, offs_h, stream)
+            tb = time.perf_counter()
             hc.decode_into(out_h, n, offs_h, mu_h, sig_d, cnt_d, back_h, stream)
+            tc = time.perf_counter()
+            if i >= 1:
+                t_enc.append(tb - ta)
+                t_dec.append(tc - tb)
         torch.cuda.synchronize(dev)
         dt = time.perf_counter() - t0
     hc.check_status("e2e")
@@ -601,6 +608,7 @@ def e2e_run(coder, w, lay, args, dev, total_bytes):
     d2h = total_bytes + 8 * (lay.n_chunks + 1) + raw
     return {"value": raw * steps / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "layers_per_batch": hc.lpb,
+            "encode_host_ms": 1e3 * float(np.median(t_enc)), "decode_host_ms": 1e3 * float(np.median(t_dec)),
             "timing": "host wall clock around skv_encode_host (host KV, mu -> host bitstream) and "
                       "skv_decode_host (host bitstream, mu -> host KV), copies overlapped with the kernels"}
 
