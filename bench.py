@@ -268,10 +268,12 @@ def main():
     sm_mhz = clocks.get("sm_mhz") or _peaks().get("sm_max_mhz", 2070.0)
     peak_tops = SMS * LANES_PER_SM_CLK * sm_mhz * 1e6 / 1e12
     achieved = ALG_OPS[(lay.dtype, dom)] * n_el / t_dom / 1e12
-    traffic = None
+    traffic = inst_per_scalar = None
     try:
         with open(args.traffic_json) as fh:
-            traffic = json.load(fh).get(f"{cfg.name}:{dom}")
+            prof = json.load(fh)
+        traffic = prof.get(f"{cfg.name}:{dom}")
+        inst_per_scalar = {k: prof.get(f"{cfg.name}:{k}:thread_inst_per_scalar") for k in ("encode", "decode")}
     except (OSError, ValueError):
         traffic = None
     hbm_peak = _peaks().get("hbm_gbs", 6685.5)
@@ -315,6 +317,7 @@ def main():
             "roofline": {"bound": "alu", "kernel": dom, "achieved": achieved, "peak": peak_tops,
                          "unit": "Tops/s", "frac": achieved / peak_tops, "traffic": traffic,
                          "alg_ops_per_scalar": ALG_OPS[(lay.dtype, dom)],
+                         "ncu_thread_inst_per_scalar": inst_per_scalar,
                          "peak_basis": f"{SMS} SMs x {LANES_PER_SM_CLK} lane-ops/clk x {sm_mhz:.0f} MHz (sampled)",
                          "hbm_bound_gbs": hbm_peak * lay.bytes_per_code / (2 * lay.bytes_per_code + bits / 8),
                          "measured_issue_tops": measured_peaks,
