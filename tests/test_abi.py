@@ -92,3 +92,23 @@ def test_library_table_generator_is_independent_and_agrees():
     lib_t = [int(x) for x in re.findall(r"(\d+)u", open(os.path.join(
         ROOT, "lossless_kv_cache_scalar_gb300", "csrc", "phi_q24.h")).read().split("*/")[1])]
     assert lib_t == [int(v) for v in O.phi_table()]
+
+
+def test_host_staging_bytes():
+    """skv_host_staging_bytes is host arithmetic: larger batches need more staging,
+    the decoder's inverse tables add 2 x 2 x 2^m bytes, and bad arguments are refused."""
+    lay = Layout("bf16", 8, 2, 8, 128, 1024)
+    lib = B.lib()
+
+    def q(lpb, op):
+        v = C.c_uint64()
+        rc = lib.skv_host_staging_bytes(C.byref(lay.c()), lpb, op, C.byref(v))
+        return rc, v.value
+
+    sizes = [q(l, 1)[1] for l in (1, 2, 4, 8)]
+    assert all(a < b for a, b in zip(sizes, sizes[1:]))
+    assert q(16, 1) == q(8, 1)                        # capped at the layer count
+    rc0, dec = q(2, 0)
+    rc2, dec_fast = q(2, 2)
+    assert rc0 == 0 and rc2 == 0 and dec_fast - dec >= 2 * (2 << 24)
+    assert q(0, 1)[0] == 1 and q(2, 7)[0] == 1
