@@ -370,9 +370,10 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
         const bool active = j < nq;
         const uint64_t q = s + (uint64_t)j * g.W;
         const float *rse = rsp + (uint32_t)((q * V) % g.HD);
-        // mu of this vector (not prefetched: the registers are worth more than
-        // the latency, which the other 31 warps hide)
+        // mu of this vector; the next one is only prefetched into L2 (a register
+        // copy of it would cost the registers the symbol loop needs)
         uint4 muv = active ? __ldg(reinterpret_cast<const uint4 *>(mup) + q) : make_uint4(0, 0, 0, 0);
+        if (j + 1 < nq) asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const uint4 *>(mup) + q + g.W));
         uint4 outv = make_uint4(0, 0, 0, 0);
         // per-symbol inputs of the next symbol, loaded one symbol ahead
         uint32_t mc_n = muv.x & MASK;
