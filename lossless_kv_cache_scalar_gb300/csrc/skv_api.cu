@@ -691,7 +691,9 @@ int32_t skv_offload_plan(const uint64_t *host_offsets, uint64_t n_chunks, uint64
     }
     if (nb < max_batches) batch_first[nb] = n_chunks;
     *n_batches = nb;
-    return nb + 1 > max_batches && max_batches ? SKV_ERR_INVALID_ARG : SKV_OK;
+    // with a plan requested, it needs nb + 1 entries (the last is n_chunks)
+    if (max_batches != 0 && max_batches < nb + 1) return SKV_ERR_INVALID_ARG;
+    return SKV_OK;
 }
 
 int32_t skv_decode_offload(const skv_layout *lay, const void *host_bitstream, uint64_t bitstream_bytes,
