@@ -140,3 +140,18 @@ def test_bad_sigma_and_nonfinite_mu_are_reported():
     with pytest.raises(O.OracleError) as e:
         O.cdf_all(O.BF16, 0x3F80, 1.0, (95, 3, 2), np.zeros(65536, np.uint64))
     assert e.value.name == "EMPTY_MARGINAL"
+
+
+@pytest.mark.parametrize("mu,sigma", [(1.5, 2.0 ** -5), (-120.0, 30.0)])
+def test_inversion_exhaustive_bf16(mu, sigma):
+    """Every one of the 2^24 bf16 slots: the oracle's search returns the o with
+    C(o) <= slot < C(o+1), i.e. numpy's searchsorted over the oracle's own C."""
+    counts = _counts(O.BF16)
+    mc = _bf16(mu)
+    c = O.cdf_all(O.BF16, mc, sigma, (95, 3, 2), counts).astype(np.uint64)
+    step = 1 << 22
+    for s0 in range(0, 1 << 24, step):
+        slots = np.arange(s0, s0 + step, dtype=np.uint64)
+        want = (np.searchsorted(c, slots, side="right") - 1).astype(np.uint32)
+        got = O.find_symbols(O.BF16, mc, sigma, slots, (95, 3, 2), counts)
+        assert np.array_equal(got, want), s0
