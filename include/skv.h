@@ -384,6 +384,20 @@ int32_t skv_requantize(uint32_t mode, uint32_t b, const void *in, uint64_t n, vo
 int32_t skv_peak_probe(int32_t kind, uint32_t iters, uint32_t *sink, uint64_t *ops, void *stream);
 
 /*
+ * The decoder's slot-to-code search on its own, for exhaustive checks: query
+ * i returns the code ordinal o with C(o) <= s < C(o+1) for s = slots[i] mod M,
+ * under predictor code mu_codes[i] and scale sigmas[i], found exactly as
+ * skv_decode finds it (the same estimate, exact test and cooperative search,
+ * the same tables: with a workspace of skv_workspace_bytes(lay, 2) the
+ * (edge, P_hat) pairs and the outlier inverse tables too), with c_out = C(o)
+ * and f_out = C(o+1) - C(o). All arrays device, n entries (uint32, float32).
+ * Device errors: NONFINITE_MU, BAD_SIGMA, EMPTY_MARGINAL.
+ */
+int32_t skv_search_eval(const skv_layout *lay, const uint64_t *counts, uint64_t n, const uint32_t *mu_codes,
+                        const float *sigmas, const uint32_t *slots, uint32_t *o_out, uint32_t *c_out,
+                        uint32_t *f_out, int32_t *status, void *workspace, uint64_t ws_bytes, void *stream);
+
+/*
  * Decode without any caller-provided scratch (the pages describe no such
  * call; it serves deployment only). Same contract and outputs as skv_decode,
  * minus the workspace arguments. It is meant for callers that cannot call

@@ -457,3 +457,22 @@ class HostCoder:
                                      C.c_void_p(self.copy_stream.cuda_stream),
                                      C.c_void_p(self.copy_out_stream.cuda_stream))
         B.check("skv_decode_host", rc)
+
+
+def search_eval(layout: Layout, counts, mu_codes, sigmas, slots, fast: bool = True, stream=None):
+    """skv_search_eval: the decoder's search for each (mu code, sigma, slot)
+    query. Returns (o, C(o), f(o)) as int64 tensors."""
+    dev = mu_codes.device
+    n = slots.numel()
+    ws = torch.empty(max(layout.workspace_bytes(False, fast), 256), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    outs = [torch.empty(n, dtype=torch.int32, device=dev) for _ in range(3)]
+    rc = B.lib().skv_search_eval(C.byref(layout.c()), _ptr(counts), n, _ptr(mu_codes), _ptr(sigmas), _ptr(slots),
+                                 _ptr(outs[0]), _ptr(outs[1]), _ptr(outs[2]), _ptr(status), _ptr(ws), ws.numel(),
+                                 _stream_handle(stream))
+    B.check("skv_search_eval", rc)
+    (stream or torch.cuda.current_stream()).synchronize()
+    st = int(status.item())
+    if st:
+        raise B.SKVError("skv_search_eval", st)
+    return tuple(o.to(torch.int64) & 0xFFFFFFFF for o in outs)

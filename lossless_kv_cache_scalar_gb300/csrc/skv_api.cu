@@ -23,6 +23,7 @@ int launch_requantize(uint32_t mode, uint32_t b, const void *in, uint64_t n, voi
                       float *s_out, uint64_t n_groups, cudaStream_t st);
 int launch_peak(int kind, uint32_t iters, uint32_t *sink, uint32_t blocks, cudaStream_t st);
 uint64_t peak_ops(int kind, uint32_t iters, uint32_t blocks);
+int launch_search_eval(const SearchArgs &sa, cudaStream_t st);
 int launch_search_aids(const Geom &g, const uint32_t *phat, float *qt, uint16_t *inv_lo,
                        uint16_t *inv_hi, cudaStream_t st);
 
@@ -980,6 +981,32 @@ int32_t skv_decode_host(const skv_layout *lay, const void *host_bits, uint64_t b
     const bool drained_all = cudaStreamSynchronize(cs) == cudaSuccess && cudaStreamSynchronize(st) == cudaSuccess &&
                              cudaStreamSynchronize(os) == cudaSuccess;
     return rc != SKV_OK ? rc : (drained_all ? SKV_OK : SKV_ERR_CUDA);
+}
+
+int32_t skv_search_eval(const skv_layout *lay, const uint64_t *counts, uint64_t n, const uint32_t *mu_codes,
+                        const float *sigmas, const uint32_t *slots, uint32_t *o_out, uint32_t *c_out,
+                        uint32_t *f_out, int32_t *status, void *workspace, uint64_t ws_bytes, void *stream) {
+    Geom g;
+    int32_t r = make_geom(lay, g);
+    if (r != SKV_OK) return r;
+    if (!status || !workspace || (g.w_h && !counts)) return SKV_ERR_INVALID_ARG;
+    if (n && (!mu_codes || !sigmas || !slots || !o_out || !c_out || !f_out)) return SKV_ERR_INVALID_ARG;
+    if (((uintptr_t)workspace & 255u) != 0 || ws_bytes < carve(g, WS_DECODE_MIN, nullptr).bytes)
+        return SKV_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return SKV_ERR_CUDA;
+    const int kind = ws_bytes >= carve(g, WS_DECODE_FULL, nullptr).bytes ? WS_DECODE_FULL : WS_DECODE_MIN;
+    const Workspace ws = carve(g, kind, static_cast<uint8_t *>(workspace));
+    Geom g1 = g;                                       // sigma is per query: no rsig
+    g1.n_planes = 0;
+    SetupArgs s{g1, nullptr, counts, ws.phat, ws.rsig, ws.ep, status};
+    if (g.dtype == SKV_BF16) setup_kernel<SKV_BF16><<<1, 1024, 0, st>>>(s);
+    else setup_kernel<SKV_E4M3><<<1, 1024, 0, st>>>(s);
+    if (cudaGetLastError() != cudaSuccess) return SKV_ERR_CUDA;
+    if (launch_search_aids(g, ws.phat, ws.qt, ws.inv_lo, ws.inv_hi, st)) return SKV_ERR_CUDA;
+    SearchArgs sa{g, ws.phat, ws.ep, ws.qt, ws.inv_lo, ws.inv_hi, n, mu_codes, sigmas, slots, o_out, c_out, f_out,
+                  status};
+    return launch_search_eval(sa, st) ? SKV_ERR_CUDA : SKV_OK;
 }
 
 }  // extern "C"

@@ -483,6 +483,93 @@ __global__ void __launch_bounds__(DecShape<DT>::warps * 32, DecShape<DT>::ctas) 
     }
 }
 
+// The decoder's search on its own: query i asks for the code of slot
+// slots[i] (taken mod M) under mu_codes[i] and sigmas[i], answered exactly as
+// decode_group answers it (the same estimate, check and cooperative search),
+// with C(o) and f(o). For exhaustive checks of the search against the model.
+template <uint32_t DT, bool EP>
+__global__ void __launch_bounds__(256) search_kernel(const SearchArgs sa) {
+    using K = Codes<DT>;
+    constexpr uint32_t M = 1u << K::m;
+    {
+        float *qt = reinterpret_cast<float *>(skv_dec_smem + kSmQt);
+        for (uint32_t i = threadIdx.x; i < kQuantFloats; i += blockDim.x) qt[i] = sa.qt[i];
+        stage_tables<DT>(*reinterpret_cast<Tables *>(skv_dec_smem + kSmPhi),
+                         *reinterpret_cast<Tables8 *>(skv_dec_smem + kSmT8), sa.phat);
+    }
+    DecArgs a{};
+    a.g = sa.g;
+    a.phat = sa.phat;
+    a.qt = sa.qt;
+    a.inv_lo = sa.inv_lo;
+    a.inv_hi = sa.inv_hi;
+    a.ep = sa.ep;
+    a.status = sa.status;
+    const Geom &g = sa.g;
+    const float kS = (float)(100.0 * 16777216.0 / (double)(M - K::N));
+    const float inv_total = (g.w_n + g.w_w) ? 1.0f / ((float)(g.w_n + g.w_w) * 16777216.0f) : 0.0f;
+    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+    bool bad_mu = false, bad_sig = false;
+    for (uint64_t base = ((uint64_t)blockIdx.x * 8u + warp) * 32u; base < sa.n;
+         base += (uint64_t)gridDim.x * 8u * 32u) {
+        const uint64_t q = base + lane;
+        const bool active = q < sa.n;
+        const uint32_t mc = active ? sa.mu_codes[q] & ((1u << (8u * K::bytes)) - 1u) : 0u;
+        const float sg = active ? sa.sigmas[q] : 1.0f;
+        const bool sok = isfinite(sg) && sg >= 1.17549435e-38f;
+        bad_sig |= active && !sok;
+        const float rs = sok ? __frcp_rn(sg) : 1.0f;
+        const bool fin = K::finite(mc);
+        bad_mu |= active && !fin;
+        const float mu = fin ? K::value(mc) : 0.0f;
+        const uint32_t slot = active ? sa.slots[q] & (M - 1u) : 0u;
+        const uint32_t o_mu = K::ord(fin ? mc : 0u);
+        const uint32_t ph = g.w_h ? phat_dec<DT, EP>(a, o_mu) : 0u;
+        uint32_t o = 0, c = 0, f = 1;
+        bool miss = false;
+        if (active) {
+            o = find_symbol<DT, EP>(a, kS, inv_total, slot, mu, rs, o_mu, ph, c, f);
+            miss = !(c <= slot && slot - c < f);
+        }
+        uint32_t pending = __ballot_sync(0xFFFFFFFFu, miss);
+        while (pending) {
+            const uint32_t Lm = __ffs(pending) - 1u;
+            pending &= pending - 1u;
+            cooperative_search<DT, EP>(a, Lm, slot, mu, rs, o, c, c + f, o, c, f);
+        }
+        if (active) {
+            sa.o_out[q] = o;
+            sa.c_out[q] = c;
+            sa.f_out[q] = f;
+        }
+    }
+    if (bad_sig) set_status(sa.status, SKV_ERR_BAD_SIGMA);
+    if (bad_mu) set_status(sa.status, SKV_ERR_NONFINITE_MU);
+}
+
+int launch_search_eval(const SearchArgs &sa, cudaStream_t st) {
+    if (sa.n == 0) return 0;
+    uint64_t blocks = (sa.n + 255u) / 256u;
+    if (blocks > 4096u) blocks = 4096u;
+    const uint32_t smem = kSmRing;                    // tables and quantiles, no word rings
+    if (sa.g.dtype == SKV_BF16) {
+        if (sa.ep) {
+            if (cudaFuncSetAttribute(search_kernel<SKV_BF16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem) != cudaSuccess) return 1;
+            search_kernel<SKV_BF16, true><<<(unsigned)blocks, 256, smem, st>>>(sa);
+        } else {
+            if (cudaFuncSetAttribute(search_kernel<SKV_BF16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem) != cudaSuccess) return 1;
+            search_kernel<SKV_BF16, false><<<(unsigned)blocks, 256, smem, st>>>(sa);
+        }
+    } else {
+        if (cudaFuncSetAttribute(search_kernel<SKV_E4M3, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess) return 1;
+        search_kernel<SKV_E4M3, false><<<(unsigned)blocks, 256, smem, st>>>(sa);
+    }
+    return cudaGetLastError() == cudaSuccess ? 0 : 1;
+}
+
 template <uint32_t DT, bool EP>
 static int launch_decode_t(const DecArgs &a, cudaStream_t st) {
     constexpr int W = DecShape<DT>::warps;

@@ -164,6 +164,21 @@ struct DecArgs {
     const uint2 *ep;       // bf16 (edge bits, P_hat) pairs, or NULL: built from the code bits
 };
 
+// Slot -> code queries through the decoder's own search (checking).
+struct SearchArgs {
+    Geom g;
+    const uint32_t *phat;
+    const uint2 *ep;           // or NULL
+    const float *qt;
+    const uint16_t *inv_lo, *inv_hi;   // or NULL
+    uint64_t n;
+    const uint32_t *mu_codes;
+    const float *sigmas;
+    const uint32_t *slots;
+    uint32_t *o_out, *c_out, *f_out;
+    int32_t *status;
+};
+
 struct CdfArgs {
     Geom g;
     const uint32_t *phat;
