@@ -26,7 +26,7 @@ template <> struct EncShape<SKV_E4M3> { static constexpr int warps = 16; };
 // No branches and no dependence on the rANS state, so the eight evaluations
 // interleave freely.
 template <uint32_t DT>
-__device__ __forceinline__ void model8(const Tables &tab, const Tables8 &tab8, const Weights w,
+__device__ __forceinline__ void model8(const TablesWide &tab, const Tables8 &tab8, const Weights w,
                                        const uint32_t *__restrict__ phat, const uint2 *__restrict__ ep,
                                        const uint4 &kvv,
                                        const uint4 &muv, const float *rsv, int e0, uint32_t *cc,
@@ -56,7 +56,7 @@ __device__ __forceinline__ void model8(const Tables &tab, const Tables8 &tab8, c
 
 // Encode one group of 32 streams (gid = chunk * G + group) with this warp.
 template <uint32_t DT>
-__device__ __forceinline__ void encode_group(const EncArgs &a, const Tables &tab, const Tables8 &tab8,
+__device__ __forceinline__ void encode_group(const EncArgs &a, const TablesWide &tab, const Tables8 &tab8,
                                              uint64_t gid) {
     using K = Codes<DT>;
     constexpr uint32_t V = K::V;
@@ -137,15 +137,17 @@ __device__ __forceinline__ void encode_group(const EncArgs &a, const Tables &tab
     if (__any_sync(0xFFFFFFFFu, overflow) && lane == 0) set_status(a.status, SKV_ERR_CAPACITY);
 }
 
-// One persistent CTA per SM: the tables are staged once; each warp's first
+// One persistent CTA per SM: the tables are staged once (the wide Phi table:
+// it saves the narrow component's clamp in every C(o)); each warp's first
 // group is warp * gridDim.x + blockIdx.x (so a small input spreads over all
 // SMs instead of filling the first CTAs), and after that each warp takes the
 // next group from a global counter until none are left, so warps stay busy
 // until the end and no CTA waits on its slowest warp.
 template <uint32_t DT>
 __global__ void __launch_bounds__(EncShape<DT>::warps * 32, 1) encode_kernel(const EncArgs a) {
-    __shared__ Tables tab;
-    __shared__ Tables8 tab8;
+    extern __shared__ __align__(16) uint8_t enc_smem[];
+    TablesWide &tab = *reinterpret_cast<TablesWide *>(enc_smem);
+    Tables8 &tab8 = *reinterpret_cast<Tables8 *>(enc_smem + sizeof(TablesWide));
     stage_tables<DT>(tab, tab8, a.phat);
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
     const uint64_t first_dynamic = (uint64_t)gridDim.x * EncShape<DT>::warps;
@@ -240,7 +242,10 @@ static int launch_encode_t(const EncArgs &a, cudaStream_t st) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return 1;
     if (blocks > (uint64_t)sms) blocks = (uint64_t)sms;
-    encode_kernel<DT><<<(unsigned)blocks, W * 32, 0, st>>>(a);
+    const int smem = (int)(sizeof(TablesWide) + sizeof(Tables8));
+    if (cudaFuncSetAttribute(encode_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return 1;
+    encode_kernel<DT><<<(unsigned)blocks, W * 32, smem, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? 0 : 1;
 }
 

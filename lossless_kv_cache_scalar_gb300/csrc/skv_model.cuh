@@ -20,10 +20,18 @@ namespace skv {
 // T[j + 2048] = round_half_even(2^24 Phi(j / 256)), FORMAT.md section 3.
 static __device__ const uint32_t kPhiQ24[4097] = {SKV_PHI_Q24_VALUES};
 
-// Tables staged in shared memory by every CTA that evaluates the model.
-struct Tables {
-    uint2 phi[4097];     // (T[j], T[j+1] - T[j]); entry 4096 = (2^24, 0)
+// Tables staged in shared memory by every CTA that evaluates the model: the
+// Phi pairs (T[j], T[j+1] - T[j]) over [-8, 8] (entry 4096 = (2^24, 0)), or,
+// WIDE, the same pairs extended over [-24, 24] with the saturated values
+// ((0, 0) below -8, (2^24, 0) from 8 on), which give the same Phi_q without
+// clamping z to [-8, 8] first (96 KB instead of 32 KB of shared memory).
+template <bool WIDE> struct PhiTables {
+    static constexpr int kCenter = WIDE ? 6144 : 2048;
+    static constexpr uint32_t kEntries = 2u * kCenter + 1u;
+    uint2 phi[kEntries];
 };
+using Tables = PhiTables<false>;
+using TablesWide = PhiTables<true>;
 struct Tables8 {         // e4m3 only: the whole alphabet fits on chip
     float edge[257];
     uint32_t phat[257];
@@ -123,12 +131,16 @@ __device__ float edge_from_values(uint32_t o) {
 }
 
 // Stage the Phi pairs (and, for e4m3, the edges and P_hat) into shared memory.
-template <uint32_t DT>
-__device__ void stage_tables(Tables &t, Tables8 &t8, const uint32_t *__restrict__ phat) {
-    for (uint32_t i = threadIdx.x; i < 4097u; i += blockDim.x) {
-        const uint32_t a = kPhiQ24[i];
-        const uint32_t b = (i < 4096u) ? kPhiQ24[i + 1] : a;
-        t.phi[i] = make_uint2(a, b - a);
+template <uint32_t DT, bool WIDE>
+__device__ void stage_tables(PhiTables<WIDE> &t, Tables8 &t8, const uint32_t *__restrict__ phat) {
+    constexpr int off = PhiTables<WIDE>::kCenter - 2048;     // entry of T[0]
+    for (uint32_t i = threadIdx.x; i < PhiTables<WIDE>::kEntries; i += blockDim.x) {
+        const int j = (int)i - off;
+        uint2 e;
+        if (j < 0) e = make_uint2(0u, 0u);
+        else if (j >= 4096) e = make_uint2(1u << 24, 0u);
+        else e = make_uint2(kPhiQ24[j], kPhiQ24[j + 1] - kPhiQ24[j]);
+        t.phi[i] = e;
     }
     if (DT == SKV_E4M3) {
         for (uint32_t o = threadIdx.x; o <= 256u; o += blockDim.x) {
@@ -141,15 +153,17 @@ __device__ void stage_tables(Tables &t, Tables8 &t8, const uint32_t *__restrict_
 
 // -------------------------------------------------------------- model: C(o)
 
-// Phi_q(zq) for zq already clamped to [-2^19, 2^19] (FORMAT.md section 3).
-__device__ __forceinline__ uint32_t phi_q(const uint2 *__restrict__ tab, int zq) {
-    const uint2 e = tab[(zq >> 8) + 2048];
+// Phi_q(zq) (FORMAT.md section 3) for zq in the table's range: [-2^19, 2^19],
+// or for the wide table [-3 2^19, 3 2^19].
+template <bool WIDE>
+__device__ __forceinline__ uint32_t phi_q(const PhiTables<WIDE> &t, int zq) {
+    const uint2 e = t.phi[(zq >> 8) + PhiTables<WIDE>::kCenter];
     return e.x + ((e.y * (uint32_t)(zq & 255)) >> 8);
 }
 
 // C(o) for an element with predictor value mu and rs = fl32(1/sigma).
-template <uint32_t DT>
-__device__ __forceinline__ uint32_t cdf(const Tables &t, const Tables8 *t8, const Weights w,
+template <uint32_t DT, bool WIDE>
+__device__ __forceinline__ uint32_t cdf(const PhiTables<WIDE> &t, const Tables8 *t8, const Weights w,
                                         const uint32_t *__restrict__ phat, uint32_t o, float mu,
                                         float rs) {
     using K = Codes<DT>;
@@ -159,12 +173,12 @@ __device__ __forceinline__ uint32_t cdf(const Tables &t, const Tables8 *t8, cons
     float z = __fmul_rn(d, rs);
     z = fminf(fmaxf(z, -24.0f), 24.0f);
     const int zq = __float2int_rd(__fmul_rn(z, 65536.0f));
-    const int zn = max(min(zq, 524288), -524288);
+    const int zn = WIDE ? zq : max(min(zq, 524288), -524288);
     // floor(zq / 3) for zq in [-3 * 2^19, 3 * 2^19]
     const int zw = (int)(__umulhi((uint32_t)(zq + 1572864), 0xAAAAAAABu) >> 1) - 524288;
     // branch-free: a zero weight multiplies its term away (P_hat is all zeros
     // when its weight is 0), so one straight-line block serves every mixture
-    const uint32_t S = w.n * phi_q(t.phi, zn) + w.w * phi_q(t.phi, zw) + w.h * K::phat(t8, phat, o);
+    const uint32_t S = w.n * phi_q(t, zn) + w.w * phi_q(t, zw) + w.h * K::phat(t8, phat, o);
     const uint64_t prod = (uint64_t)S * MN;
     return o + (uint32_t)(prod >> 24) / 100u;
 }
@@ -173,7 +187,8 @@ __device__ __forceinline__ uint32_t cdf(const Tables &t, const Tables8 *t8, cons
 // from the per-call table ep (ep[o] = (bits of E(o), P_hat(o))) instead of
 // being rebuilt from the code bits: one 8-byte load replaces the edge's
 // integer work and the P_hat load.
-__device__ __forceinline__ uint32_t cdf_ep(const Tables &t, const Weights w,
+template <bool WIDE>
+__device__ __forceinline__ uint32_t cdf_ep(const PhiTables<WIDE> &t, const Weights w,
                                            const uint2 *__restrict__ ep, uint32_t o, float mu,
                                            float rs) {
     constexpr uint32_t MN = (1u << 24) - 65536u;
@@ -182,9 +197,9 @@ __device__ __forceinline__ uint32_t cdf_ep(const Tables &t, const Weights w,
     float z = __fmul_rn(d, rs);
     z = fminf(fmaxf(z, -24.0f), 24.0f);
     const int zq = __float2int_rd(__fmul_rn(z, 65536.0f));
-    const int zn = max(min(zq, 524288), -524288);
+    const int zn = WIDE ? zq : max(min(zq, 524288), -524288);
     const int zw = (int)(__umulhi((uint32_t)(zq + 1572864), 0xAAAAAAABu) >> 1) - 524288;
-    const uint32_t S = w.n * phi_q(t.phi, zn) + w.w * phi_q(t.phi, zw) + w.h * e.y;
+    const uint32_t S = w.n * phi_q(t, zn) + w.w * phi_q(t, zw) + w.h * e.y;
     const uint64_t prod = (uint64_t)S * MN;
     return o + (uint32_t)(prod >> 24) / 100u;
 }
