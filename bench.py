@@ -142,7 +142,9 @@ def run_reference(args, cfg):
             "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32/u64 int + f32",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": cfg.name, "sample": desc},
+            "config": {"workload": cfg.name, "shape": [cfg.n_layers, cfg.n_kv, cfg.n_tokens, cfg.n_heads,
+                                                       cfg.head_dim],
+                       "code_dtype": cfg.dtype, "scalars": cfg.n_elems, "sample": desc},
             "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
