@@ -41,33 +41,29 @@ __device__ __forceinline__ uint4 lower_unit(const uint32_t (&w)[8]) {
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// B = 4 (8 -> 4 bits), the same arithmetic two codes at a time: the even and
-// odd bytes of a word go to two 16-bit lanes, where q + 8 <= 263 and every
-// intermediate stays within its lane (no carries or borrows cross lanes).
+// B = 4 (8 -> 4 bits), the same arithmetic four codes at a time, one per
+// byte of a word. With q = 16 hi + lo: t = q + 8 gives a = t >> 4 = hi +
+// [lo >= 8] <= 16 and c = t mod 16 = (lo + 8) mod 16, and every intermediate
+// (lo + 8 <= 23, c + 16 - a in [0, 31], a + x >= 1) stays inside its byte.
 template <uint32_t MODE>
 __device__ __forceinline__ uint32_t lower4_word(uint32_t w) {
-    uint32_t r[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const uint32_t q = (w >> (8 * h)) & 0x00FF00FFu;          // codes 2i + h in two lanes
-        uint32_t v;
-        if (MODE == 1) {
-            v = (q >> 4) & 0x000F000Fu;
-        } else if (MODE == 2) {
-            const uint32_t t = q + 0x00080008u;
-            v = (t >> 4) & 0x001F001Fu;                              // <= 16
-            v -= (v >> 4) & 0x00010001u;                             // min(., 15)
+    const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu, lo = w & 0x0F0F0F0Fu;
+    uint32_t r;
+    if (MODE == 1) {
+        r = hi;                                                      // q >> 4
+    } else {
+        const uint32_t lo8 = lo + 0x08080808u;
+        const uint32_t a = hi + ((lo8 >> 4) & 0x01010101u);           // (q + 8) >> 4
+        if (MODE == 2) {
+            r = a - ((a >> 4) & 0x01010101u);                         // min(a, 15)
         } else {
-            const uint32_t t = q + 0x00080008u;
-            const uint32_t a = (t >> 4) & 0x0FFF0FFFu;               // t >> 4 per lane, <= 16
-            const uint32_t c = t & 0x000F000Fu;                      // t mod 16
-            const uint32_t x = ((c + 0x00100010u - a) >> 4) & 0x00010001u;   // [c >= a]
-            v = a + x - 0x00010001u;                                 // a - [a > c]
+            const uint32_t c = lo8 & 0x0F0F0F0Fu;
+            const uint32_t x = ((c + 0x10101010u - a) >> 4) & 0x01010101u;   // [c >= a]
+            r = a + x - 0x01010101u;                                  // a - [a > c]
         }
-        r[h] = v;
     }
-    const uint32_t m = r[0] | (r[1] << 4);                           // bytes 0 and 2: two codes each
-    return (m & 0xFFu) | ((m >> 8) & 0xFF00u);
+    const uint32_t t = r | (r >> 4);                                  // codes 0|1 in byte 0, 2|3 in byte 2
+    return (t & 0xFFu) | ((t >> 8) & 0xFF00u);
 }
 
 template <uint32_t B, uint32_t MODE>
