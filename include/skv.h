@@ -242,6 +242,29 @@ int32_t skv_decode_offload(const skv_layout *lay, const void *host_bitstream, ui
                            void *stream, void *copy_stream);
 
 /*
+ * Random-access page decode from host memory: the pages (chunks) listed in
+ * host_chunk_ids are copied from the host bitstream into the staging buffer
+ * on copy_stream (one copy per page) and decoded on stream, with the tables
+ * skv_decode_prepare built in the workspace (as skv_decode_chunks_prepared).
+ * The KV stays compressed in host memory and only the pages a request needs
+ * cross the link (the offload use of the wiki's uses section).
+ *  host_bitstream, host_offsets  host, as skv_encode wrote them
+ *  host_chunk_ids  host uint32[n_ids], each < n_chunks (else SKV_ERR_INVALID_ARG)
+ *  pages_out       device, as skv_decode_chunks
+ *  staging         device, 256-byte aligned: 4 n_ids and 8 (n_ids + 1) bytes (each
+ *                  rounded up to 256) plus the listed pages' bytes, else
+ *                  SKV_ERR_INVALID_ARG; it must not be reused until stream has
+ *                  finished this call's work
+ * Offsets that descend, pass bitstream_bytes or are not 16-byte multiples
+ * return SKV_ERR_CORRUPT. Device errors as skv_decode_chunks_prepared.
+ */
+int32_t skv_decode_pages_host(const skv_layout *lay, const void *host_bitstream, uint64_t bitstream_bytes,
+                              const uint64_t *host_offsets, const void *mu, const uint32_t *host_chunk_ids,
+                              uint32_t n_ids, void *pages_out, int32_t *status, const void *workspace,
+                              uint64_t ws_bytes, void *staging, uint64_t staging_bytes, void *stream,
+                              void *copy_stream);
+
+/*
  * The batch plan skv_decode_offload follows (host only, no CUDA call): cut
  * chunks 0..n_chunks-1 into runs of whole chunks of at most batch_bytes bytes
  * and (if max_chunks > 0) at most max_chunks chunks each, in order, each run

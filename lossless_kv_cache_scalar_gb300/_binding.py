@@ -55,6 +55,8 @@ SIGNATURES = {
     "skv_decode_host": (_i32, [_LP, _vp, _u64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _u64, _u32, _vp, _vp, _vp]),
     "skv_search_eval": (_i32, [_LP, _vp, _u64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _u64, _vp]),
     "skv_peak_probe": (_i32, [_i32, _u32, _vp, C.POINTER(_u64), _vp]),
+    "skv_decode_pages_host": (_i32, [_LP, _vp, _u64, _vp, _vp, _vp, _u32, _vp, _vp, _vp, _u64, _vp, _u64, _vp,
+                                     _vp]),
     "skv_offload_plan": (_i32, [_vp, _u64, _u64, _u64, _vp, _u64, C.POINTER(_u64)]),
     "skv_calibrate_sigma": (_i32, [_LP, _vp, _vp, _vp, _u64, _vp, _vp]),
 }

@@ -262,6 +262,33 @@ class Coder:
         B.check("skv_decode_offload", rc)
         return cs
 
+    def decode_pages_host_into(self, host_bitstream, host_offsets, mu, host_ids, pages_out, staging,
+                               stream=None, copy_stream=None):
+        """Enqueue skv_decode_pages_host: the listed pages, read from a (pinned) host
+        bitstream, decoded with the tables of prepare_decode. host_ids: CPU int32."""
+        lay = self.layout
+        if host_bitstream.is_cuda or host_offsets.is_cuda or host_ids.is_cuda:
+            raise ValueError("host_bitstream, host_offsets and host_ids must be CPU tensors")
+        if host_ids.dtype != torch.int32 or not host_ids.is_contiguous():
+            raise ValueError("host_ids must be a contiguous int32 CPU tensor")
+        if host_offsets.dtype != torch.int64 or host_offsets.numel() != self.n_chunks + 1:
+            raise ValueError("host_offsets must be the int64 CPU offsets (n_chunks + 1)")
+        if pages_out.numel() != host_ids.numel() * lay.page_elems:
+            raise ValueError("pages_out must hold n_ids * tokens_per_chunk * HD codes")
+        if not staging.is_cuda or staging.dtype != torch.uint8:
+            raise ValueError("staging must be a uint8 CUDA tensor")
+        _check_codes(mu, lay, "mu")
+        cs = copy_stream if copy_stream is not None else torch.cuda.Stream(device=mu.device)
+        rc = B.lib().skv_decode_pages_host(C.byref(self._c), C.c_void_p(host_bitstream.data_ptr()),
+                                           host_bitstream.numel() * host_bitstream.element_size(),
+                                           C.c_void_p(host_offsets.data_ptr()), _ptr(mu),
+                                           C.c_void_p(host_ids.data_ptr()), host_ids.numel(), _ptr(pages_out),
+                                           _ptr(self.status), _ptr(self.workspace), self.workspace.numel(),
+                                           _ptr(staging), staging.numel(), _stream_handle(stream),
+                                           C.c_void_p(cs.cuda_stream))
+        B.check("skv_decode_pages_host", rc)
+        return cs
+
     def decode_chunks(self, bitstream, offsets, mu, sigma, counts, chunk_ids, stream=None):
         lay = self.layout
         pages = torch.zeros((chunk_ids.numel(), lay.page_elems), dtype=mu.dtype, device=mu.device)

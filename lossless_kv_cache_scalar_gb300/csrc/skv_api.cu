@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
+#include <vector>
 
 #include "skv_model.cuh"
 
@@ -531,7 +532,7 @@ static int32_t decode_launch(const Geom &g, const void *bitstream, uint64_t bits
     DecArgs da{g, static_cast<const uint8_t *>(bitstream), bitstream_bytes, offsets,
                static_cast<const uint8_t *>(mu), ws.phat, ws.rsig, ws.qt, ws.inv_lo, ws.inv_hi,
                pages ? ids : nullptr,
-               n_units, static_cast<uint8_t *>(out), (uint64_t)g.Tc * g.HD, status, 0, 0, ws.ep};
+               n_units, static_cast<uint8_t *>(out), (uint64_t)g.Tc * g.HD, status, 0, 0, ws.ep, nullptr};
     return launch_decode(da, st) ? SKV_ERR_CUDA : SKV_OK;
 }
 
@@ -757,7 +758,7 @@ int32_t skv_decode_offload(const skv_layout *lay, const void *host_bitstream, ui
         if (ok) {
             DecArgs da{g, dst, bytes, offsets, static_cast<const uint8_t *>(mu), ws.phat, ws.rsig, ws.qt,
                        ws.inv_lo, ws.inv_hi, nullptr, k1 - k0, static_cast<uint8_t *>(kv_out),
-                       (uint64_t)g.Tc * g.HD, status, o0, k0, ws.ep};
+                       (uint64_t)g.Tc * g.HD, status, o0, k0, ws.ep, nullptr};
             ok = launch_decode(da, st) == 0;
         }
         if (ok) ok = cudaEventRecord(freed[h], st) == cudaSuccess;
@@ -970,7 +971,7 @@ int32_t skv_decode_host(const skv_layout *lay, const void *host_bits, uint64_t b
         if (!ok) { rc = SKV_ERR_CUDA; break; }
         DecArgs da{gs, hs.bits[h], nbytes, hs.offs[h], hs.mu[h], ws.phat,
                    ws.rsig + (uint64_t)l0 * lay->n_kv * g.n_sblk * g.HD, ws.qt, ws.inv_lo, ws.inv_hi, nullptr,
-                   gs.n_chunks, hs.kv[h], (uint64_t)g.Tc * g.HD, status, o0, 0, ws.ep};
+                   gs.n_chunks, hs.kv[h], (uint64_t)g.Tc * g.HD, status, o0, 0, ws.ep, nullptr};
         if (launch_decode(da, st) || cudaEventRecord(decoded.e[h], st) != cudaSuccess) { rc = SKV_ERR_CUDA; break; }
         ok = cudaStreamWaitEvent(os, decoded.e[h], 0) == cudaSuccess;
         ok = ok && cudaMemcpyAsync(static_cast<uint8_t *>(host_kv_out) + e0 * d.bytes, hs.kv[h], ne * d.bytes,
@@ -1007,6 +1008,67 @@ int32_t skv_search_eval(const skv_layout *lay, const uint64_t *counts, uint64_t 
     SearchArgs sa{g, ws.phat, ws.ep, ws.qt, ws.inv_lo, ws.inv_hi, n, mu_codes, sigmas, slots, o_out, c_out, f_out,
                   status};
     return launch_search_eval(sa, st) ? SKV_ERR_CUDA : SKV_OK;
+}
+
+int32_t skv_decode_pages_host(const skv_layout *lay, const void *host_bitstream, uint64_t bitstream_bytes,
+                              const uint64_t *host_offsets, const void *mu, const uint32_t *host_chunk_ids,
+                              uint32_t n_ids, void *pages_out, int32_t *status, const void *workspace,
+                              uint64_t ws_bytes, void *staging, uint64_t staging_bytes, void *stream,
+                              void *copy_stream) {
+    Geom g;
+    int32_t r = make_geom(lay, g);
+    if (r != SKV_OK) return r;
+    if (!status || !workspace || ((uintptr_t)workspace & 255u) != 0) return SKV_ERR_INVALID_ARG;
+    if (ws_bytes < carve(g, WS_DECODE_MIN, nullptr).bytes) return SKV_ERR_INVALID_ARG;
+    if (n_ids == 0) return SKV_OK;
+    if (!host_bitstream || !host_offsets || !host_chunk_ids || !mu || !pages_out || !staging ||
+        ((uintptr_t)staging & 255u) || !aligned16(mu) || !aligned16(pages_out))
+        return SKV_ERR_INVALID_ARG;
+    // staging: [chunk ids][per-page byte offsets][the pages' bytes, back to back]
+    const uint64_t ids_bytes = round256(4ull * n_ids), offs_bytes = round256(8ull * (n_ids + 1ull));
+    if (staging_bytes < ids_bytes + offs_bytes) return SKV_ERR_INVALID_ARG;
+    std::vector<uint64_t> uoff(n_ids + 1ull);
+    uoff[0] = 0;
+    for (uint32_t i = 0; i < n_ids; ++i) {
+        const uint64_t k = host_chunk_ids[i];
+        if (k >= g.n_chunks) return SKV_ERR_INVALID_ARG;
+        const uint64_t a = host_offsets[k], b = host_offsets[k + 1];
+        if (b < a || b > bitstream_bytes || ((a | b) & 15u)) return SKV_ERR_CORRUPT;
+        uoff[i + 1] = uoff[i] + (b - a);
+    }
+    if (ids_bytes + offs_bytes + uoff[n_ids] > staging_bytes) return SKV_ERR_INVALID_ARG;
+    uint8_t *base = static_cast<uint8_t *>(staging);
+    uint32_t *d_ids = reinterpret_cast<uint32_t *>(base);
+    uint64_t *d_off = reinterpret_cast<uint64_t *>(base + ids_bytes);
+    uint8_t *d_bits = base + ids_bytes + offs_bytes;
+    cudaStream_t st = static_cast<cudaStream_t>(stream), cs = static_cast<cudaStream_t>(copy_stream);
+    cudaEvent_t copied = nullptr;
+    if (cudaEventCreateWithFlags(&copied, cudaEventDisableTiming) != cudaSuccess) return SKV_ERR_CUDA;
+    bool ok = cudaMemsetAsync(status, 0, sizeof(int32_t), st) == cudaSuccess;
+    // the staging may still be read by this stream's previous decode
+    cudaEvent_t prior = nullptr;
+    ok = ok && cudaEventCreateWithFlags(&prior, cudaEventDisableTiming) == cudaSuccess;
+    ok = ok && cudaEventRecord(prior, st) == cudaSuccess && cudaStreamWaitEvent(cs, prior, 0) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(d_ids, host_chunk_ids, 4ull * n_ids, cudaMemcpyHostToDevice, cs) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(d_off, uoff.data(), 8ull * (n_ids + 1ull), cudaMemcpyHostToDevice, cs) == cudaSuccess;
+    for (uint32_t i = 0; i < n_ids && ok; ++i) {
+        const uint64_t k = host_chunk_ids[i];
+        ok = cudaMemcpyAsync(d_bits + uoff[i], static_cast<const uint8_t *>(host_bitstream) + host_offsets[k],
+                             uoff[i + 1] - uoff[i], cudaMemcpyHostToDevice, cs) == cudaSuccess;
+    }
+    ok = ok && cudaEventRecord(copied, cs) == cudaSuccess && cudaStreamWaitEvent(st, copied, 0) == cudaSuccess;
+    int32_t rc = ok ? SKV_OK : SKV_ERR_CUDA;
+    if (ok) {
+        const int kind = ws_bytes >= carve(g, WS_DECODE_FULL, nullptr).bytes ? WS_DECODE_FULL : WS_DECODE_MIN;
+        const Workspace ws = carve(g, kind, static_cast<uint8_t *>(const_cast<void *>(workspace)));
+        DecArgs da{g, d_bits, uoff[n_ids], nullptr, static_cast<const uint8_t *>(mu), ws.phat, ws.rsig, ws.qt,
+                   ws.inv_lo, ws.inv_hi, d_ids, n_ids, static_cast<uint8_t *>(pages_out),
+                   (uint64_t)g.Tc * g.HD, status, 0, 0, ws.ep, d_off};
+        rc = launch_decode(da, st) ? SKV_ERR_CUDA : SKV_OK;
+    }
+    if (prior) cudaEventDestroy(prior);
+    cudaEventDestroy(copied);
+    return rc;
 }
 
 }  // extern "C"

@@ -314,7 +314,10 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
         return;
     }
     const ChunkSpan cs = chunk_span(g, k);
-    const uint64_t o0 = a.offsets[k], o1 = a.offsets[k + 1];
+    // the chunk's bytes: by chunk id from the offsets table, or (pages gathered
+    // into a buffer of their own) by unit from a per-unit table
+    const uint64_t o0 = a.unit_offsets ? a.unit_offsets[unit] : a.offsets[k];
+    const uint64_t o1 = a.unit_offsets ? a.unit_offsets[unit + 1] : a.offsets[k + 1];
     const uint64_t off0 = o0 - a.origin, off1 = o1 - a.origin;
     if (o0 < a.origin || o0 > o1 || off1 > a.stream_bytes || (off0 & 15u) || off1 - off0 < g.hdr_bytes) {
         if (lane == 0) set_status(a.status, SKV_ERR_CORRUPT);

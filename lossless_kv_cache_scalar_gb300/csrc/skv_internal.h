@@ -162,6 +162,7 @@ struct DecArgs {
     uint64_t origin;       // stream holds the bytes from offset `origin` on (staged decode)
     uint64_t chunk0;       // without ids: unit u decodes chunk chunk0 + u
     const uint2 *ep;       // bf16 (edge bits, P_hat) pairs, or NULL: built from the code bits
+    const uint64_t *unit_offsets;   // or NULL: unit u's bytes are [unit_offsets[u], unit_offsets[u+1])
 };
 
 // Slot -> code queries through the decoder's own search (checking).

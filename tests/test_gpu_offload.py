@@ -95,3 +95,33 @@ def test_offload_rejects_small_staging_and_bad_offsets():
     with pytest.raises(SKVError) as e:
         c.check_status("offload")
     assert e.value.name == "CORRUPT"
+
+
+@pytest.mark.parametrize("name,layers,tokens,kw", [
+    ("qwen3_0p6b", 2, 1024, {}),
+    ("fp8_32b", 2, 700, dict(tokens_per_chunk=100, streams_per_chunk=96)),
+    ("paged_14b", 1, 2048, dict(streams_per_chunk=256)),
+])
+def test_pages_from_host_equal_device_pages(name, layers, tokens, kw):
+    """skv_decode_pages_host: listed pages read from the host bitstream decode
+    to the same pages as skv_decode_chunks on the device stream, in list order,
+    duplicates and the last (shorter) page included."""
+    lay, w, c, s, offs, host, host_offs = _encoded(name, layers, tokens, **kw)
+    c.prepare_decode(w["sigma"], w["counts"])
+    rng = np.random.default_rng(11)
+    n = lay.n_chunks
+    ids = np.concatenate([rng.integers(0, n, 9), [n - 1, 0, n - 1]]).astype(np.int32)
+    sizes = np.diff(host_offs.numpy())
+    staging = torch.empty(int(sizes[ids].sum()) + 4096, dtype=torch.uint8, device="cuda")
+    pages = torch.zeros((ids.size, lay.page_elems), dtype=w["mu"].dtype, device="cuda")
+    c.decode_pages_host_into(host, host_offs, w["mu"], torch.from_numpy(ids), pages, staging)
+    c.check_status("pages from host")
+    want = c.decode_chunks(s, offs, w["mu"], w["sigma"], w["counts"], torch.from_numpy(ids).cuda())
+    assert torch.equal(pages, want)
+    # a staging buffer one page short is refused before anything is copied
+    short = torch.empty(int(sizes[ids].sum()) - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(SKVError):
+        c.decode_pages_host_into(host, host_offs, w["mu"], torch.from_numpy(ids), pages, short)
+    with pytest.raises(SKVError):
+        bad = torch.tensor([0, n], dtype=torch.int32)
+        c.decode_pages_host_into(host, host_offs, w["mu"], bad, pages[:2], staging)
