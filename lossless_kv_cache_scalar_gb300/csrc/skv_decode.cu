@@ -41,6 +41,11 @@ static_assert(DecShape<SKV_BF16>::warps * DecShape<SKV_BF16>::ctas == (int)kDecR
 constexpr uint32_t kRing = 256;        // words per warp ring
 constexpr uint32_t kBlock = 64;        // words per cp.async batch (16 B per lane, 16 lanes)
 constexpr uint32_t kStepSyms = 4;      // the ring is topped up every 4 symbols
+// per warp: the word ring, then a 512-byte stage holding each lane's 16-byte
+// vector of mu codes, transposed ([word][lane]) so lanes hit distinct banks;
+// decoded codes overwrite their mu codes in place
+constexpr uint32_t kStageWords = 4u * 32u;
+constexpr uint32_t kWarpSmem = kRing + kStageWords;   // 32-bit words
 
 // dynamic shared memory layout (bytes)
 constexpr uint32_t kSmPhi = 0;                                        // Tables
@@ -48,7 +53,9 @@ constexpr uint32_t kSmQt = (sizeof(Tables) + 15u) & ~15u;              // float2
 constexpr uint32_t kSmT8 = (kSmQt + 8u * (kQuantN + 1) + 15u) & ~15u;  // Tables8
 constexpr uint32_t kSmRing = (kSmT8 + sizeof(Tables8) + 15u) & ~15u;   // uint32 [warps][kRing]
 template <uint32_t DT>
-constexpr uint32_t dec_smem() { return kSmRing + DecShape<DT>::warps * kRing * 4u; }
+constexpr uint32_t dec_smem() { return kSmRing + DecShape<DT>::warps * kWarpSmem * 4u; }
+static_assert(dec_smem<SKV_BF16>() <= 227u * 1024u && dec_smem<SKV_E4M3>() <= 227u * 1024u,
+              "decoder shared memory above the per-CTA limit");
 
 // ------------------------------------------------------------ search aids
 
@@ -303,7 +310,6 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
     constexpr uint32_t M = 1u << m;
     constexpr uint64_t L = K::L;
     constexpr uint32_t BITS = 8u * K::bytes;
-    constexpr uint32_t MASK = (1u << BITS) - 1u;
     const Geom &g = a.g;
     const uint32_t lane = threadIdx.x & 31u;
     const uint64_t unit = gid / g.G;
@@ -367,22 +373,36 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
     uint32_t filled = 0;    // words requested into the ring so far (warp-uniform)
 
 
+    uint32_t *stage = ring + kRing;              // [4 words][32 lanes]
     for (int64_t j = 0; j < nq0; ++j) {
         const bool active = j < nq;
         const uint64_t q = s + (uint64_t)j * g.W;
         const float *rse = rsp + (uint32_t)((q * V) % g.HD);
-        // mu of this vector; the next one is only prefetched into L2 (a register
-        // copy of it would cost the registers the symbol loop needs)
-        uint4 muv = active ? __ldg(reinterpret_cast<const uint4 *>(mup) + q) : make_uint4(0, 0, 0, 0);
+        // mu of this vector into the lane's stage column; the next vector is
+        // only prefetched into L2
+        {
+            const uint4 muv = active ? __ldg(reinterpret_cast<const uint4 *>(mup) + q) : make_uint4(0, 0, 0, 0);
+            stage[0 * 32 + lane] = muv.x;
+            stage[1 * 32 + lane] = muv.y;
+            stage[2 * 32 + lane] = muv.z;
+            stage[3 * 32 + lane] = muv.w;
+        }
         if (j + 1 < nq) asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const uint4 *>(mup) + q + g.W));
-        uint4 outv = make_uint4(0, 0, 0, 0);
+        // code e of the lane's vector in the stage: word e / (32 / BITS), part e mod (32 / BITS)
+        auto at = [&](uint32_t e) -> uint32_t {
+            constexpr uint32_t per = 32u / BITS;
+            return ((e / per) * 32u + lane) * per + (e % per);
+        };
+        auto get = [&](uint32_t e) -> uint32_t {
+            return BITS == 16 ? reinterpret_cast<const uint16_t *>(stage)[at(e)]
+                              : reinterpret_cast<const uint8_t *>(stage)[at(e)];
+        };
         // per-symbol inputs of the next symbol, loaded one symbol ahead
-        uint32_t mc_n = muv.x & MASK;
+        uint32_t mc_n = get(0);
         float rs_n = active ? __ldg(rse) : 1.0f;
         uint32_t ph_n = (active && g.w_h) ? phat_dec<DT, EP>(a, K::ord(K::finite(mc_n) ? mc_n : 0u)) : 0u;
         // One symbol per iteration, unrolled four times (1% faster than twice)
-        // while the loop body still fits the instruction cache; mu codes shift
-        // out of the bottom of the vector and decoded codes shift in at the top.
+        // while the loop body still fits the instruction cache.
 #pragma unroll 4
         for (uint32_t e = 0; e < V; ++e) {
             if ((e & (kStepSyms - 1u)) == 0u) {
@@ -403,16 +423,12 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
             const uint32_t mc = mc_n;
             const float rs = rs_n;
             const uint32_t ph = ph_n;
-            muv.x = __funnelshift_r(muv.x, muv.y, BITS);
-            muv.y = __funnelshift_r(muv.y, muv.z, BITS);
-            muv.z = __funnelshift_r(muv.z, muv.w, BITS);
-            muv.w >>= BITS;
             if (e + 1u < V && active) {
-                mc_n = muv.x & MASK;
+                mc_n = get(e + 1u);
                 rs_n = __ldg(rse + e + 1u);
                 if (g.w_h) ph_n = phat_dec<DT, EP>(a, K::ord(K::finite(mc_n) ? mc_n : 0u));
             }
-            uint32_t code = 0, slot = 0, o = 0, c = 0, f = 1;
+            uint32_t slot = 0, o = 0, c = 0, f = 1;
             float mu = 0.0f;
             bool miss = false;
             if (active) {
@@ -432,12 +448,10 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
             }
             if (active) {
                 x = (uint64_t)f * (x >> m) + slot - c;
-                code = K::code(o);
+                // the decoded code replaces its (already read) mu code
+                if (BITS == 16) reinterpret_cast<uint16_t *>(stage)[at(e)] = (uint16_t)K::code(o);
+                else reinterpret_cast<uint8_t *>(stage)[at(e)] = (uint8_t)K::code(o);
             }
-            outv.x = __funnelshift_r(outv.x, outv.y, BITS);
-            outv.y = __funnelshift_r(outv.y, outv.z, BITS);
-            outv.z = __funnelshift_r(outv.z, outv.w, BITS);
-            outv.w = (outv.w >> BITS) | (code << (32u - BITS));
             const bool refill = active && x < L;
             const uint32_t ball = __ballot_sync(0xFFFFFFFFu, refill);
             if (ball) {
@@ -451,7 +465,9 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
                 rp += __popc(ball);
             }
         }
-        if (active) reinterpret_cast<uint4 *>(outp)[q] = outv;
+        if (active)
+            reinterpret_cast<uint4 *>(outp)[q] =
+                make_uint4(stage[0 * 32 + lane], stage[1 * 32 + lane], stage[2 * 32 + lane], stage[3 * 32 + lane]);
     }
     cp_async_wait0();
     corrupt |= (x != L);
@@ -475,7 +491,7 @@ __global__ void __launch_bounds__(DecShape<DT>::warps * 32, DecShape<DT>::ctas) 
                          *reinterpret_cast<Tables8 *>(skv_dec_smem + kSmT8), a.phat);
     }
     const uint32_t warp = threadIdx.x >> 5;
-    uint32_t *ring = reinterpret_cast<uint32_t *>(skv_dec_smem + kSmRing) + warp * kRing;
+    uint32_t *ring = reinterpret_cast<uint32_t *>(skv_dec_smem + kSmRing) + warp * kWarpSmem;
     const uint64_t n_groups = a.n_units * a.g.G;
     for (uint64_t gid = (uint64_t)warp * gridDim.x + blockIdx.x; gid < n_groups;
          gid += (uint64_t)gridDim.x * kDecWarps) {
