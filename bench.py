@@ -166,8 +166,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", default="qwen3_8b")
     ap.add_argument("--impl", default="skv", choices=["skv", "reference"])
-    ap.add_argument("--ref-chunks", type=int, default=8, help="chunks per oracle step")
-    ap.add_argument("--cpu-chunks", type=int, default=16, help="chunks in the cpu_baseline sample")
+    ap.add_argument("--ref-chunks", type=int, default=32, help="chunks per oracle step")
+    ap.add_argument("--cpu-chunks", type=int, default=128,
+                    help="chunks in the cpu_baseline sample (about 15 core-seconds of oracle work on 16 cores)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-layers", type=int, default=0,
                     help="layers per batch of the host pipelines (0: the library's default, four batches)")
