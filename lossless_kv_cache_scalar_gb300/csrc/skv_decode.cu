@@ -401,8 +401,8 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
         uint32_t mc_n = get(0);
         float rs_n = active ? __ldg(rse) : 1.0f;
         uint32_t ph_n = (active && g.w_h) ? phat_dec<DT, EP>(a, K::ord(K::finite(mc_n) ? mc_n : 0u)) : 0u;
-        // One symbol per iteration, unrolled four times (1% faster than twice)
-        // while the loop body still fits the instruction cache.
+        // One symbol per iteration, unrolled four times: 1% faster than twice;
+        // eight times is slower by a quarter (more values live across the body).
 #pragma unroll 4
         for (uint32_t e = 0; e < V; ++e) {
             if ((e & (kStepSyms - 1u)) == 0u) {
