@@ -66,7 +66,9 @@ enum {
  *  dtype              SKV_BF16 or SKV_E4M3
  *  n_layers, n_kv     planes; n_kv is 2 for K and V
  *  n_heads, head_dim  HD = n_heads * head_dim channels; HD * bytes_per_code % 16 == 0
- *  n_tokens           T (may be 0)
+ *  n_tokens           T (may be 0), at most 2^40; n_layers * n_kv * T * HD (the
+ *                     scalars) at most 2^48 and the sigma table at most 2^40
+ *                     entries, so that no size the library computes overflows
  *  tokens_per_chunk   page length T_c >= 1; a chunk is one (layer, kv, page) and
  *                     decodes independently (the random-access unit)
  *  streams_per_chunk  W = 32 * G, G in 1..8: interleaved rANS streams per chunk

@@ -163,6 +163,15 @@ static int32_t make_geom(const skv_layout *lay, Geom &g) {
     const uint64_t HD = (uint64_t)lay->n_heads * lay->head_dim;
     if ((HD * d.bytes) % 16 != 0 || HD > (1ull << 24)) return SKV_ERR_INVALID_ARG;
     if (lay->n_tokens > (1ull << 40)) return SKV_ERR_INVALID_ARG;
+    {
+        // every size below is a product of these: bound them so none overflows
+        const unsigned __int128 planes = (unsigned __int128)lay->n_layers * lay->n_kv;
+        const uint64_t nsb = lay->sigma_block_tokens
+                                 ? (lay->n_tokens + lay->sigma_block_tokens - 1) / lay->sigma_block_tokens
+                                 : 1u;
+        if (planes * lay->n_tokens * HD > ((unsigned __int128)1 << 48)) return SKV_ERR_INVALID_ARG;
+        if (planes * nsb * HD > ((unsigned __int128)1 << 40)) return SKV_ERR_INVALID_ARG;
+    }
     std::memset(&g, 0, sizeof g);
     g.dtype = lay->dtype;
     g.n_kv = lay->n_kv;

@@ -50,7 +50,10 @@ def test_layout_init_and_checks():
     assert (lay.tokens_per_chunk, lay.streams_per_chunk) == (256, 64)
     assert (lay.w_narrow, lay.w_wide, lay.w_marginal) == (95, 3, 2)
     bad = [dict(streams_per_chunk=48), dict(streams_per_chunk=288), dict(tokens_per_chunk=0),
-           dict(w_marginal=3), dict(version=2), dict(dtype=5), dict(n_heads=1, head_dim=4), dict(sigma_block_tokens=100)]
+           dict(w_marginal=3), dict(version=2), dict(dtype=5), dict(n_heads=1, head_dim=4), dict(sigma_block_tokens=100),
+           dict(n_tokens=(1 << 40) + 1),                                   # T above 2^40
+           dict(n_layers=1 << 20, n_kv=1 << 10),                           # 2^30 planes x 2^15 x 2^10 scalars
+           dict(n_layers=0xFFFFFFFF, n_kv=0xFFFFFFFF, n_tokens=0)]         # empty, but 2^64 planes of sigma
     for kw in bad:
         l2 = B.skv_layout()
         C.memmove(C.byref(l2), C.byref(lay), C.sizeof(lay))
