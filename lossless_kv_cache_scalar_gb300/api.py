@@ -113,6 +113,21 @@ def _check_model_inputs(lay: Layout, sigma: torch.Tensor, counts: torch.Tensor |
         raise ValueError(f"counts must be a contiguous int64 CUDA tensor of {lay.n_codes} entries")
 
 
+def _check_dev(t, what: str, dtype=None, numel=None, min_numel=None, elem_size=None):
+    """A device buffer handed to the C ABI as a bare pointer: contiguous, on the
+    GPU, of the given dtype or element size, and large enough."""
+    if t is None or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{what} must be a contiguous CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{what} must be {dtype}")
+    if elem_size is not None and t.element_size() != elem_size:
+        raise ValueError(f"{what} must have {elem_size}-byte elements")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{what} must have {numel} elements")
+    if min_numel is not None and t.numel() < min_numel:
+        raise ValueError(f"{what} must have at least {min_numel} elements")
+
+
 def _check_codes(t: torch.Tensor, lay: Layout, what: str):
     if not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{what} must be a contiguous CUDA tensor")
@@ -141,6 +156,15 @@ class Coder:
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.n_chunks = layout.n_chunks
 
+    def _check_stream_and_offsets(self, bitstream, offsets):
+        _check_dev(bitstream, "bitstream", torch.uint8)
+        _check_dev(offsets, "offsets", torch.int64, numel=self.n_chunks + 1)
+
+    def _check_pages(self, chunk_ids, pages_out):
+        _check_dev(chunk_ids, "chunk_ids", torch.int32)
+        _check_dev(pages_out, "pages_out", elem_size=self.layout.bytes_per_code,
+                   numel=chunk_ids.numel() * self.layout.page_elems)
+
     # -- status
     def check_status(self, where: str, stream=None):
         (stream or torch.cuda.current_stream()).synchronize()
@@ -161,6 +185,8 @@ class Coder:
         _check_codes(kv, lay, "kv")
         _check_codes(mu, lay, "mu")
         _check_model_inputs(lay, sigma, counts)
+        _check_dev(out, "out", torch.uint8)
+        _check_dev(offsets, "offsets", torch.int64, numel=self.n_chunks + 1)
         rc = B.lib().skv_encode(C.byref(self._c), _ptr(kv), _ptr(mu), _ptr(sigma), _ptr(counts),
                                 _ptr(out), out.numel(), _ptr(offsets), _ptr(self.status),
                                 _ptr(self.workspace), self.workspace.numel(),
@@ -181,6 +207,7 @@ class Coder:
         _check_codes(mu, lay, "mu")
         _check_codes(kv_out, lay, "kv_out")
         _check_model_inputs(lay, sigma, counts)
+        self._check_stream_and_offsets(bitstream, offsets)
         rc = B.lib().skv_decode(C.byref(self._c), _ptr(bitstream), bitstream.numel(),
                                 _ptr(offsets), _ptr(mu), _ptr(sigma), _ptr(counts), _ptr(kv_out),
                                 _ptr(self.status), _ptr(self.workspace), self.workspace.numel(),
@@ -197,10 +224,8 @@ class Coder:
                            stream=None):
         lay = self.layout
         ids = chunk_ids
-        if ids.dtype != torch.int32 or not ids.is_cuda:
-            raise ValueError("chunk_ids must be an int32 CUDA tensor")
-        if pages_out.numel() != ids.numel() * lay.page_elems:
-            raise ValueError("pages_out must hold n_ids * tokens_per_chunk * HD codes")
+        self._check_pages(ids, pages_out)
+        self._check_stream_and_offsets(bitstream, offsets)
         _check_codes(mu, lay, "mu")
         _check_model_inputs(lay, sigma, counts)
         rc = B.lib().skv_decode_chunks(C.byref(self._c), _ptr(bitstream), bitstream.numel(),
@@ -222,10 +247,9 @@ class Coder:
 
     def decode_chunks_prepared_into(self, bitstream, offsets, mu, chunk_ids, pages_out, stream=None):
         lay = self.layout
-        if chunk_ids.dtype != torch.int32 or not chunk_ids.is_cuda:
-            raise ValueError("chunk_ids must be an int32 CUDA tensor")
-        if pages_out.numel() != chunk_ids.numel() * lay.page_elems:
-            raise ValueError("pages_out must hold n_ids * tokens_per_chunk * HD codes")
+        self._check_pages(chunk_ids, pages_out)
+        self._check_stream_and_offsets(bitstream, offsets)
+        _check_codes(mu, lay, "mu")
         rc = B.lib().skv_decode_chunks_prepared(C.byref(self._c), _ptr(bitstream), bitstream.numel(),
                                                 _ptr(offsets), _ptr(mu), _ptr(chunk_ids),
                                                 chunk_ids.numel(), _ptr(pages_out), _ptr(self.status),
@@ -244,8 +268,7 @@ class Coder:
         if host_offsets.dtype != torch.int64 or host_offsets.numel() != self.n_chunks + 1 \
                 or not host_offsets.is_contiguous() or not host_bitstream.is_contiguous():
             raise ValueError("host_offsets must be a contiguous int64 CPU tensor of n_chunks + 1")
-        if offsets.numel() != self.n_chunks + 1 or not offsets.is_cuda:
-            raise ValueError("offsets must be the device offsets (n_chunks + 1)")
+        _check_dev(offsets, "offsets", torch.int64, numel=self.n_chunks + 1)
         if not staging.is_cuda or staging.dtype != torch.uint8 or not staging.is_contiguous():
             raise ValueError("staging must be a contiguous uint8 CUDA tensor")
         _check_codes(mu, lay, "mu")
@@ -271,12 +294,11 @@ class Coder:
             raise ValueError("host_bitstream, host_offsets and host_ids must be CPU tensors")
         if host_ids.dtype != torch.int32 or not host_ids.is_contiguous():
             raise ValueError("host_ids must be a contiguous int32 CPU tensor")
-        if host_offsets.dtype != torch.int64 or host_offsets.numel() != self.n_chunks + 1:
-            raise ValueError("host_offsets must be the int64 CPU offsets (n_chunks + 1)")
-        if pages_out.numel() != host_ids.numel() * lay.page_elems:
-            raise ValueError("pages_out must hold n_ids * tokens_per_chunk * HD codes")
-        if not staging.is_cuda or staging.dtype != torch.uint8:
-            raise ValueError("staging must be a uint8 CUDA tensor")
+        if host_offsets.dtype != torch.int64 or host_offsets.numel() != self.n_chunks + 1 \
+                or not host_offsets.is_contiguous() or not host_bitstream.is_contiguous():
+            raise ValueError("host_offsets must be the contiguous int64 CPU offsets (n_chunks + 1)")
+        _check_dev(pages_out, "pages_out", elem_size=lay.bytes_per_code, numel=host_ids.numel() * lay.page_elems)
+        _check_dev(staging, "staging", torch.uint8)
         _check_codes(mu, lay, "mu")
         cs = copy_stream if copy_stream is not None else torch.cuda.Stream(device=mu.device)
         rc = B.lib().skv_decode_pages_host(C.byref(self._c), C.c_void_p(host_bitstream.data_ptr()),
@@ -297,10 +319,21 @@ class Coder:
         return pages
 
 
+def _check_query(layout: Layout, counts, n: int, **bufs):
+    """Per-query arrays of cdf_eval / search_eval: n 4-byte entries each."""
+    if counts is not None:
+        _check_dev(counts, "counts", torch.int64, numel=layout.n_codes)
+    elif layout.weights[2]:
+        raise ValueError("counts are needed when the marginal weight is nonzero")
+    for name, t in bufs.items():
+        _check_dev(t, name, elem_size=4, numel=n)
+
+
 def cdf_eval(layout: Layout, counts, mu_codes, sigmas, ords, stream=None) -> torch.Tensor:
     """C(o) per query via skv_cdf_eval (uint32 results as int64 tensor)."""
     dev = mu_codes.device
     n = ords.numel()
+    _check_query(layout, counts, n, mu_codes=mu_codes, sigmas=sigmas, ords=ords)
     ws = torch.empty(max(layout.workspace_bytes(False), 256), dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     out = torch.empty(n, dtype=torch.int32, device=dev)
@@ -404,7 +437,7 @@ def requantize(codes: torch.Tensor, n: int, b: int, scale: torch.Tensor, group: 
     if codes.numel() * 8 < n * 2 * b:
         raise ValueError("codes holds fewer than n codes of 2b bits")
     n_groups = -(-n // group)
-    if scale.dtype != torch.float32 or not scale.is_cuda or scale.numel() < n_groups:
+    if scale.dtype != torch.float32 or not scale.is_cuda or not scale.is_contiguous() or scale.numel() < n_groups:
         raise ValueError("scale must be a float32 CUDA tensor with one entry per group")
     out = torch.empty(max(n * b // 8, 16), dtype=torch.uint8, device=codes.device)
     s_out = torch.empty(max(n_groups, 1), dtype=torch.float32, device=codes.device)
@@ -491,6 +524,7 @@ def search_eval(layout: Layout, counts, mu_codes, sigmas, slots, fast: bool = Tr
     query. Returns (o, C(o), f(o)) as int64 tensors."""
     dev = mu_codes.device
     n = slots.numel()
+    _check_query(layout, counts, n, mu_codes=mu_codes, sigmas=sigmas, slots=slots)
     ws = torch.empty(max(layout.workspace_bytes(False, fast), 256), dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     outs = [torch.empty(n, dtype=torch.int32, device=dev) for _ in range(3)]

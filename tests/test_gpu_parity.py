@@ -240,6 +240,43 @@ def test_decode_chunks_rejects_bad_id():
     assert e.value.name == "INVALID_ARG"
 
 
+def test_binding_rejects_bad_buffers():
+    """The C ABI takes bare pointers, so the binding refuses buffers that are too
+    short, of the wrong element size or not contiguous before any call."""
+    cfg = synth.CONFIGS["tiny"]
+    wd, _ = _workload(cfg)
+    lay = H.layout_of(cfg)
+    c = Coder(lay)
+    s, offs = c.encode(wd["kv"], wd["mu"], wd["sigma"], wd["counts"])
+    args = (wd["mu"], wd["sigma"], wd["counts"])
+    with pytest.raises(ValueError):                        # offsets one entry short
+        c.decode(s, offs[:-1], *args)
+    with pytest.raises(ValueError):                        # offsets as int32
+        c.decode(s, offs.to(torch.int32), *args)
+    with pytest.raises(ValueError):                        # bitstream not bytes
+        c.decode(s[: s.numel() // 4 * 4].view(torch.int32), offs, *args)
+    out, o2 = c.alloc_output()
+    with pytest.raises(ValueError):                        # encoder offsets too short
+        c.encode_into(wd["kv"], wd["mu"], wd["sigma"], wd["counts"], out, o2[:1])
+    ids = torch.tensor([0, 1], dtype=torch.int32, device="cuda")
+    half = torch.empty(2 * lay.page_elems, dtype=torch.uint8, device="cuda")   # 1-byte codes for bf16
+    with pytest.raises(ValueError):
+        c.decode_chunks_into(s, offs, *args, ids, half)
+    strided = torch.tensor([0, 9, 1, 9], dtype=torch.int32, device="cuda")[::2]
+    pages = torch.empty((2, lay.page_elems), dtype=wd["mu"].dtype, device="cuda")
+    with pytest.raises(ValueError):                        # non-contiguous ids
+        c.decode_chunks_into(s, offs, *args, strided, pages)
+    c.prepare_decode(wd["sigma"], wd["counts"])
+    with pytest.raises(ValueError):                        # mu of the wrong size
+        c.decode_chunks_prepared_into(s, offs, wd["mu"].view(-1)[:16], ids, pages)
+    with pytest.raises(ValueError):                        # query arrays of unequal length
+        cdf_eval(lay, wd["counts"], torch.zeros(3, dtype=torch.int32, device="cuda"),
+                 torch.ones(2, dtype=torch.float32, device="cuda"), torch.zeros(3, dtype=torch.int32, device="cuda"))
+    # and the valid call still works
+    c.decode_chunks_prepared_into(s, offs, wd["mu"], ids, pages)
+    c.check_status("pages")
+
+
 # ------------------------------------------------------------------ errors
 
 def test_status_errors():
