@@ -31,11 +31,14 @@ int launch_search_aids(const Geom &g, const uint32_t *phat, float *qt, uint16_t 
 // ------------------------------------------------------------- set-up kernel
 
 // P_hat(o) = floor(2^24 cum(o) / total) exactly (FORMAT.md section 5): a
-// binary64 estimate, then integer correction with 128-bit products.
-__device__ uint32_t phat_entry(uint64_t cum, uint64_t total) {
+// binary32 estimate cum * (2^24 / total), within a few units of the result,
+// then integer correction with 128-bit products. `scale` = 2^24 / total is
+// computed once per thread (binary64 division is slow, and the set-up builds
+// all entries on one SM).
+__device__ uint32_t phat_entry(uint64_t cum, uint64_t total, float scale) {
     const unsigned __int128 lhs = (unsigned __int128)cum << 24;
-    double est = (double)cum / (double)total * 16777216.0;
-    uint32_t p = est >= 16777216.0 ? 16777216u : (uint32_t)est;
+    const float est = __fmul_rn(__ull2float_rn(cum), scale);
+    uint32_t p = est >= 16777216.0f ? 16777216u : (uint32_t)est;
     while (p < 16777216u && (unsigned __int128)(p + 1u) * total <= lhs) ++p;
     while (p > 0u && (unsigned __int128)p * total > lhs) --p;
     return p;
@@ -72,18 +75,18 @@ __global__ void __launch_bounds__(1024) setup_kernel(const SetupArgs a) {
             if (DT == SKV_BF16 && a.ep) a.ep[o] = make_uint2(__float_as_uint(K::edge(nullptr, o)), 0u);
         }
     } else {
-        constexpr uint32_t per = (K::N + 1023u) / 1024u;
-        const uint32_t o0 = tid * per, o1 = min(o0 + per, K::N);
-        uint64_t local = 0;
-        for (uint32_t o = o0; o < o1; ++o) local += a.counts[K::code(o)];
+        // Each warp owns a contiguous range of code orders and walks it 32 at
+        // a time (coalesced): pass 1 sums the range, a scan of the 32 warp sums
+        // gives each range its starting count, and pass 2 scans each step of 32
+        // with shuffles, carrying the running count, and writes P_hat.
+        constexpr uint32_t span = (K::N + 31u) / 32u;          // orders per warp (blockDim 1024)
         const uint32_t lane = tid & 31u, warp = tid >> 5;
-        uint64_t incl = local;
+        const uint32_t r0 = warp * span, r1 = min(r0 + span, K::N);
+        uint64_t local = 0;
+        for (uint32_t o = r0 + lane; o < r1; o += 32u) local += a.counts[K::code(o)];
 #pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const uint64_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-            if (lane >= (uint32_t)d) incl += v;
-        }
-        if (lane == 31) warp_tot[warp] = incl;
+        for (int d = 16; d > 0; d >>= 1) local += __shfl_xor_sync(0xFFFFFFFFu, local, d);
+        if (lane == 0) warp_tot[warp] = local;
         __syncthreads();
         if (warp == 0) {
             uint64_t t = warp_tot[lane];
@@ -96,7 +99,6 @@ __global__ void __launch_bounds__(1024) setup_kernel(const SetupArgs a) {
         }
         __syncthreads();
         const uint64_t total = warp_tot[31];
-        uint64_t cum = (warp ? warp_tot[warp - 1] : 0ull) + incl - local;
         if (total == 0) {
             for (uint32_t o = tid; o <= K::N; o += blockDim.x) {
                 a.phat[o] = 0u;
@@ -104,11 +106,23 @@ __global__ void __launch_bounds__(1024) setup_kernel(const SetupArgs a) {
             }
             if (tid == 0) set_status(a.status, SKV_ERR_EMPTY_MARGINAL);
         } else {
-            for (uint32_t o = o0; o < o1; ++o) {
-                const uint32_t p = phat_entry(cum, total);
-                a.phat[o] = p;
-                if (DT == SKV_BF16 && a.ep) a.ep[o] = make_uint2(__float_as_uint(K::edge(nullptr, o)), p);
-                cum += a.counts[K::code(o)];
+            const float scale = (float)(16777216.0 / (double)total);
+            uint64_t carry = warp ? warp_tot[warp - 1] : 0ull;  // cum(r0)
+            for (uint32_t b = r0; b < r1; b += 32u) {
+                const uint32_t o = b + lane;
+                const uint64_t c = o < r1 ? a.counts[K::code(o)] : 0ull;
+                uint64_t incl = c;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const uint64_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+                    if (lane >= (uint32_t)d) incl += v;
+                }
+                if (o < r1) {
+                    const uint32_t p = phat_entry(carry + incl - c, total, scale);
+                    a.phat[o] = p;
+                    if (DT == SKV_BF16 && a.ep) a.ep[o] = make_uint2(__float_as_uint(K::edge(nullptr, o)), p);
+                }
+                carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
             }
             if (tid == 0) {
                 a.phat[K::N] = 1u << 24;

@@ -207,11 +207,20 @@ __global__ void __launch_bounds__(1024) scan_kernel(const ScanArgs a) {
 }
 
 // Copy each chunk's states, word counts and words to its place in the stream.
-__global__ void __launch_bounds__(256) compact_kernel(const CompactArgs a) {
+// The words of all the chunk's groups form one run of 16-byte units (each
+// group's words padded to 4), so the whole CTA copies them at once: a thread
+// gathers four words per unit from the group's scratch slot (which starts at
+// any word) and writes the unit with one 16-byte store, four units in flight.
+constexpr int kCompactThreads = 512;
+constexpr int kCompactUnroll = 4;
+
+__global__ void __launch_bounds__(kCompactThreads) compact_kernel(const CompactArgs a) {
     const Geom &g = a.g;
+    __shared__ uint32_t s_nw[8];        // words of each group (G <= 8)
+    __shared__ uint64_t s_unit[9];      // first unit of each group, then the total
     for (uint64_t k = blockIdx.x; k < g.n_chunks; k += gridDim.x) {
         const uint64_t off = a.offsets[k], end = a.offsets[k + 1];
-        if (end > a.out_capacity) continue;
+        if (end > a.out_capacity) continue;            // same for the whole CTA
         uint8_t *dst = a.out + off;
         uint64_t *st = reinterpret_cast<uint64_t *>(dst);
         for (uint32_t i = threadIdx.x; i < g.W; i += blockDim.x) st[i] = a.states[k * g.W + i];
@@ -219,16 +228,44 @@ __global__ void __launch_bounds__(256) compact_kernel(const CompactArgs a) {
         const uint32_t hwords = (uint32_t)(pad16(4ull * g.G) / 4);
         for (uint32_t i = threadIdx.x; i < hwords; i += blockDim.x)
             hw[i] = i < g.G ? a.nwords[k * g.G + i] : 0u;
-        uint64_t pos = g.hdr_bytes;
-        for (uint32_t j = 0; j < g.G; ++j) {
-            const uint64_t gid = k * g.G + j;
-            const uint32_t nw = a.nwords[gid];
-            const uint32_t *src = a.scratch + gid * g.cap_words + (g.cap_words - nw);
-            uint32_t *dw = reinterpret_cast<uint32_t *>(dst + pos);
-            const uint32_t padded = (nw + 3u) & ~3u;
-            for (uint32_t i = threadIdx.x; i < padded; i += blockDim.x) dw[i] = i < nw ? src[i] : 0u;
-            pos += 4ull * padded;
+        if (threadIdx.x == 0) {
+            uint64_t u = 0;
+            for (uint32_t j = 0; j < g.G; ++j) {
+                const uint32_t nw = a.nwords[k * g.G + j];
+                s_nw[j] = nw;
+                s_unit[j] = u;
+                u += (nw + 3u) / 4u;
+            }
+            s_unit[g.G] = u;
         }
+        __syncthreads();
+        const uint64_t units = s_unit[g.G];
+        uint4 *dst4 = reinterpret_cast<uint4 *>(dst + g.hdr_bytes);
+        for (uint64_t u0 = threadIdx.x; u0 < units; u0 += (uint64_t)kCompactUnroll * blockDim.x) {
+            uint4 v[kCompactUnroll];
+#pragma unroll
+            for (int r = 0; r < kCompactUnroll; ++r) {
+                const uint64_t u = u0 + (uint64_t)r * blockDim.x;
+                v[r] = make_uint4(0u, 0u, 0u, 0u);
+                if (u < units) {
+                    uint32_t j = 0;
+                    while (j + 1 < g.G && s_unit[j + 1] <= u) ++j;
+                    const uint32_t nw = s_nw[j];
+                    const uint32_t i = 4u * (uint32_t)(u - s_unit[j]);
+                    const uint32_t *src = a.scratch + (k * g.G + j) * g.cap_words + (g.cap_words - nw);
+                    v[r].x = src[i];                           // i < nw: a unit holds at least one word
+                    v[r].y = i + 1u < nw ? src[i + 1u] : 0u;
+                    v[r].z = i + 2u < nw ? src[i + 2u] : 0u;
+                    v[r].w = i + 3u < nw ? src[i + 3u] : 0u;
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < kCompactUnroll; ++r) {
+                const uint64_t u = u0 + (uint64_t)r * blockDim.x;
+                if (u < units) dst4[u] = v[r];
+            }
+        }
+        __syncthreads();                               // s_nw / s_unit are rewritten for the next chunk
     }
 }
 
@@ -261,7 +298,7 @@ int launch_scan(const ScanArgs &a, cudaStream_t st) {
 int launch_compact(const CompactArgs &a, cudaStream_t st) {
     if (a.g.n_chunks == 0) return 0;
     const uint64_t blocks = a.g.n_chunks < 65535u ? a.g.n_chunks : 65535u;
-    compact_kernel<<<(unsigned)blocks, 256, 0, st>>>(a);
+    compact_kernel<<<(unsigned)blocks, kCompactThreads, 0, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? 0 : 1;
 }
 
