@@ -44,14 +44,36 @@ __device__ uint32_t phat_entry(uint64_t cum, uint64_t total, float scale) {
     return p;
 }
 
-// All CTAs validate sigma and write rsig = fl32(1/sigma) (grid-stride); CTA 0
-// also builds P_hat in code order from the marginal histogram.
+// Orders of P_hat built by one set-up CTA (one per thread).
+constexpr uint32_t kSetupThreads = 1024;
+
+// Block-wide sum of one uint64 per thread (blockDim kSetupThreads); `red` is
+// 32 words of shared memory. Every thread gets the sum.
+__device__ uint64_t block_sum(uint64_t v, uint64_t *red) {
+    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, d);
+    __syncthreads();                                  // red may still be read from a previous use
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    uint64_t t = red[lane];
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, d);
+    return t;
+}
+
+// All CTAs validate sigma and write rsig = fl32(1/sigma) (grid-stride). CTA b
+// < ceil(N / 1024) also builds P_hat for the code orders [1024 b, 1024 b +
+// 1024): it sums the whole histogram (the total) and the part below its range
+// (its starting count), both from L2, then scans its 1,024 counts, one per
+// thread, coalesced. Spread over CTAs this way the exact entries (128-bit
+// products) are not all computed on one SM.
 template <uint32_t DT>
-__global__ void __launch_bounds__(1024) setup_kernel(const SetupArgs a) {
+__global__ void __launch_bounds__(kSetupThreads) setup_kernel(const SetupArgs a) {
     using K = Codes<DT>;
     const Geom &g = a.g;
     const uint32_t tid = threadIdx.x;
-    __shared__ uint64_t warp_tot[32];
+    __shared__ uint64_t red[32];
     __shared__ int bad_sigma;
     if (tid == 0) bad_sigma = 0;
     __syncthreads();
@@ -63,68 +85,63 @@ __global__ void __launch_bounds__(1024) setup_kernel(const SetupArgs a) {
         a.rsig[i] = ok ? __frcp_rn(sg) : 1.0f;
         if (!ok) bad_sigma = 1;
     }
-    if (blockIdx.x != 0) {
-        __syncthreads();
-        if (tid == 0 && bad_sigma) set_status(a.status, SKV_ERR_BAD_SIGMA);
-        return;
-    }
 
-    if (g.w_h == 0) {
-        for (uint32_t o = tid; o <= K::N; o += blockDim.x) {
-            a.phat[o] = 0u;
-            if (DT == SKV_BF16 && a.ep) a.ep[o] = make_uint2(__float_as_uint(K::edge(nullptr, o)), 0u);
-        }
-    } else {
-        // Each warp owns a contiguous range of code orders and walks it 32 at
-        // a time (coalesced): pass 1 sums the range, a scan of the 32 warp sums
-        // gives each range its starting count, and pass 2 scans each step of 32
-        // with shuffles, carrying the running count, and writes P_hat.
-        constexpr uint32_t span = (K::N + 31u) / 32u;          // orders per warp (blockDim 1024)
-        const uint32_t lane = tid & 31u, warp = tid >> 5;
-        const uint32_t r0 = warp * span, r1 = min(r0 + span, K::N);
-        uint64_t local = 0;
-        for (uint32_t o = r0 + lane; o < r1; o += 32u) local += a.counts[K::code(o)];
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) local += __shfl_xor_sync(0xFFFFFFFFu, local, d);
-        if (lane == 0) warp_tot[warp] = local;
-        __syncthreads();
-        if (warp == 0) {
-            uint64_t t = warp_tot[lane];
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const uint64_t v = __shfl_up_sync(0xFFFFFFFFu, t, d);
-                if (lane >= (uint32_t)d) t += v;
+    const uint32_t o0 = blockIdx.x * kSetupThreads;
+    if (o0 < K::N) {
+        const uint32_t o = o0 + tid;                  // this thread's order
+        const bool mine = o < K::N;
+        uint64_t total = 0, base = 0;
+        if (g.w_h) {
+            uint64_t t = 0, b = 0;
+            for (uint32_t q = tid; q < K::N; q += kSetupThreads) {
+                const uint64_t c = a.counts[K::code(q)];
+                t += c;
+                if (q < o0) b += c;
             }
-            warp_tot[lane] = t;
+            total = block_sum(t, red);
+            base = block_sum(b, red);
         }
-        __syncthreads();
-        const uint64_t total = warp_tot[31];
-        if (total == 0) {
-            for (uint32_t o = tid; o <= K::N; o += blockDim.x) {
+        if (total == 0) {                             // no marginal term, or an empty histogram
+            if (mine) {
                 a.phat[o] = 0u;
                 if (DT == SKV_BF16 && a.ep) a.ep[o] = make_uint2(__float_as_uint(K::edge(nullptr, o)), 0u);
             }
-            if (tid == 0) set_status(a.status, SKV_ERR_EMPTY_MARGINAL);
+            if (blockIdx.x == 0 && tid == 0) {
+                a.phat[K::N] = 0u;
+                if (DT == SKV_BF16 && a.ep) a.ep[K::N] = make_uint2(__float_as_uint(K::edge(nullptr, K::N)), 0u);
+                if (g.w_h) set_status(a.status, SKV_ERR_EMPTY_MARGINAL);
+            }
         } else {
-            const float scale = (float)(16777216.0 / (double)total);
-            uint64_t carry = warp ? warp_tot[warp - 1] : 0ull;  // cum(r0)
-            for (uint32_t b = r0; b < r1; b += 32u) {
-                const uint32_t o = b + lane;
-                const uint64_t c = o < r1 ? a.counts[K::code(o)] : 0ull;
-                uint64_t incl = c;
+            // exclusive scan of this CTA's counts, one per thread
+            const uint32_t lane = tid & 31u, warp = tid >> 5;
+            const uint64_t c = mine ? a.counts[K::code(o)] : 0ull;
+            uint64_t incl = c;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const uint64_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+                if (lane >= (uint32_t)d) incl += v;
+            }
+            __syncthreads();
+            if (lane == 31) red[warp] = incl;
+            __syncthreads();
+            if (warp == 0) {
+                uint64_t t = red[lane];
 #pragma unroll
                 for (int d = 1; d < 32; d <<= 1) {
-                    const uint64_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-                    if (lane >= (uint32_t)d) incl += v;
+                    const uint64_t v = __shfl_up_sync(0xFFFFFFFFu, t, d);
+                    if (lane >= (uint32_t)d) t += v;
                 }
-                if (o < r1) {
-                    const uint32_t p = phat_entry(carry + incl - c, total, scale);
-                    a.phat[o] = p;
-                    if (DT == SKV_BF16 && a.ep) a.ep[o] = make_uint2(__float_as_uint(K::edge(nullptr, o)), p);
-                }
-                carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+                red[lane] = t;
             }
-            if (tid == 0) {
+            __syncthreads();
+            const uint64_t cum = base + (warp ? red[warp - 1] : 0ull) + incl - c;
+            if (mine) {
+                const float scale = (float)(16777216.0 / (double)total);
+                const uint32_t p = phat_entry(cum, total, scale);
+                a.phat[o] = p;
+                if (DT == SKV_BF16 && a.ep) a.ep[o] = make_uint2(__float_as_uint(K::edge(nullptr, o)), p);
+            }
+            if (blockIdx.x == 0 && tid == 0) {
                 a.phat[K::N] = 1u << 24;
                 if (DT == SKV_BF16 && a.ep) a.ep[K::N] = make_uint2(__float_as_uint(K::edge(nullptr, K::N)), 1u << 24);
             }
@@ -132,6 +149,22 @@ __global__ void __launch_bounds__(1024) setup_kernel(const SetupArgs a) {
     }
     __syncthreads();
     if (tid == 0 && bad_sigma) set_status(a.status, SKV_ERR_BAD_SIGMA);
+}
+
+// The set-up grid: enough CTAs for P_hat and for the sigmas, at most 1,024.
+template <uint32_t DT>
+static int launch_setup_t(const SetupArgs &s, cudaStream_t st) {
+    const uint64_t nsig = s.g.n_planes * s.g.n_sblk * s.g.HD;
+    uint64_t grid = (Codes<DT>::N + kSetupThreads - 1) / kSetupThreads;
+    const uint64_t gs = (nsig + 65535u) / 65536u;       // 64 sigmas per thread at most
+    if (gs > grid) grid = gs;
+    if (grid > 1024u) grid = 1024u;
+    setup_kernel<DT><<<(unsigned)grid, kSetupThreads, 0, st>>>(s);
+    return cudaGetLastError() == cudaSuccess ? 0 : 1;
+}
+
+static int launch_setup(const SetupArgs &s, cudaStream_t st) {
+    return s.g.dtype == SKV_BF16 ? launch_setup_t<SKV_BF16>(s, st) : launch_setup_t<SKV_E4M3>(s, st);
 }
 
 // C(o) for independent (mu, sigma, o) queries (model-kernel checks).
@@ -303,12 +336,7 @@ static Workspace carve(const Geom &g, int kind, uint8_t *base) {
 static int32_t run_setup(const Geom &g, const float *sigma, const uint64_t *counts,
                          const Workspace &ws, int32_t *status, cudaStream_t st) {
     SetupArgs s{g, sigma, counts, ws.phat, ws.rsig, ws.ep, status};
-    // one CTA per 64 Ki sigmas beyond the first (CTA 0 also builds P_hat)
-    const uint64_t nsig = g.n_planes * g.n_sblk * g.HD;
-    const unsigned grid = (unsigned)(1 + (nsig > 65536 ? (nsig - 65536 + 65535) / 65536 : 0));
-    if (g.dtype == SKV_BF16) setup_kernel<SKV_BF16><<<grid < 1024 ? grid : 1024, 1024, 0, st>>>(s);
-    else setup_kernel<SKV_E4M3><<<grid < 1024 ? grid : 1024, 1024, 0, st>>>(s);
-    return cudaGetLastError() == cudaSuccess ? SKV_OK : SKV_ERR_CUDA;
+    return launch_setup(s, st) ? SKV_ERR_CUDA : SKV_OK;
 }
 
 static int32_t common_checks(const Geom &g, const float *sigma, const uint64_t *counts,
@@ -656,9 +684,7 @@ int32_t skv_cdf_eval(const skv_layout *lay, const uint64_t *counts, uint64_t n,
     Geom g1 = g;
     g1.n_planes = 0;
     SetupArgs s{g1, nullptr, counts, ws.phat, ws.rsig, nullptr, status};
-    if (g.dtype == SKV_BF16) setup_kernel<SKV_BF16><<<1, 1024, 0, st>>>(s);
-    else setup_kernel<SKV_E4M3><<<1, 1024, 0, st>>>(s);
-    if (cudaGetLastError() != cudaSuccess) return SKV_ERR_CUDA;
+    if (launch_setup(s, st)) return SKV_ERR_CUDA;
     if (n == 0) return SKV_OK;
     CdfArgs ca{g, ws.phat, n, mu_codes, sigmas, ords, C_out, status};
     const uint64_t blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
@@ -851,11 +877,7 @@ int32_t skv_encode_host(const skv_layout *lay, const void *host_kv, const void *
     // tables for the whole cache, once (P_hat, 1/sigma, bf16 pairs)
     SetupArgs sa{g, sigma, counts, hs.phat, hs.rsig, hs.ep, status};
     {
-        const uint64_t nsig = g.n_planes * g.n_sblk * g.HD;
-        const unsigned grid = (unsigned)(1 + (nsig > 65536 ? (nsig - 65536 + 65535) / 65536 : 0));
-        if (g.dtype == SKV_BF16) setup_kernel<SKV_BF16><<<grid < 1024 ? grid : 1024, 1024, 0, st>>>(sa);
-        else setup_kernel<SKV_E4M3><<<grid < 1024 ? grid : 1024, 1024, 0, st>>>(sa);
-        if (cudaGetLastError() != cudaSuccess) return SKV_ERR_CUDA;
+        if (launch_setup(sa, st)) return SKV_ERR_CUDA;
     }
     const DtypeInfo d = dtype_info(g.dtype);
     const uint64_t plane_elems = g.T * g.HD;
@@ -961,11 +983,7 @@ int32_t skv_decode_host(const skv_layout *lay, const void *host_bits, uint64_t b
     ws.phat = hs.phat; ws.rsig = hs.rsig; ws.qt = hs.qt; ws.inv_lo = hs.inv_lo; ws.inv_hi = hs.inv_hi; ws.ep = hs.ep;
     {
         SetupArgs sa{g, sigma, counts, ws.phat, ws.rsig, ws.ep, status};
-        const uint64_t nsig = g.n_planes * g.n_sblk * g.HD;
-        const unsigned grid = (unsigned)(1 + (nsig > 65536 ? (nsig - 65536 + 65535) / 65536 : 0));
-        if (g.dtype == SKV_BF16) setup_kernel<SKV_BF16><<<grid < 1024 ? grid : 1024, 1024, 0, st>>>(sa);
-        else setup_kernel<SKV_E4M3><<<grid < 1024 ? grid : 1024, 1024, 0, st>>>(sa);
-        if (cudaGetLastError() != cudaSuccess) return SKV_ERR_CUDA;
+        if (launch_setup(sa, st)) return SKV_ERR_CUDA;
         if (launch_search_aids(g, ws.phat, ws.qt, ws.inv_lo, ws.inv_hi, st)) return SKV_ERR_CUDA;
     }
     const DtypeInfo d = dtype_info(g.dtype);
@@ -1024,9 +1042,7 @@ int32_t skv_search_eval(const skv_layout *lay, const uint64_t *counts, uint64_t 
     Geom g1 = g;                                       // sigma is per query: no rsig
     g1.n_planes = 0;
     SetupArgs s{g1, nullptr, counts, ws.phat, ws.rsig, ws.ep, status};
-    if (g.dtype == SKV_BF16) setup_kernel<SKV_BF16><<<1, 1024, 0, st>>>(s);
-    else setup_kernel<SKV_E4M3><<<1, 1024, 0, st>>>(s);
-    if (cudaGetLastError() != cudaSuccess) return SKV_ERR_CUDA;
+    if (launch_setup(s, st)) return SKV_ERR_CUDA;
     if (launch_search_aids(g, ws.phat, ws.qt, ws.inv_lo, ws.inv_hi, st)) return SKV_ERR_CUDA;
     SearchArgs sa{g, ws.phat, ws.ep, ws.qt, ws.inv_lo, ws.inv_hi, n, mu_codes, sigmas, slots, o_out, c_out, f_out,
                   status};
