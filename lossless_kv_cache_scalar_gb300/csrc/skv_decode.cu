@@ -195,11 +195,14 @@ __device__ __forceinline__ uint32_t estimate(const DecArgs &a, float kS, float i
     const float ph_top = (float)(a.g.w_h << 24) - ph;
     // the quantile of the Gaussian part, measured from whichever end is nearer
     const int d = (int)s - (int)o_ref;
-    below = fmaf((float)d, kS, -ph) * inv_total <= 0.5f;
+    below = fmaf((float)d, kS, -ph) <= 0.5f / inv_total;     // the divide is loop-invariant
     const int dd = below ? max(d, 0) : max(MN - d, 0);
     const float gt = fmaxf(fmaf((float)dd, kS, below ? -ph : -ph_top) * inv_total, 0.0f);
     far = gt < 9.094947e-13f;                       // 2^-40
-    const float u = fminf(fmaxf(fmaf(-__log2f(gt), (float)kQuantSteps, -(float)kQuantSteps), 0.0f),
+    // an estimate only: lg2 without subnormal handling (a subnormal gt is far)
+    float lg;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(gt));
+    const float u = fminf(fmaxf(fmaf(-lg, (float)kQuantSteps, -(float)kQuantSteps), 0.0f),
                           (float)kQuantN - 0.001f);
     const int k = (int)u;
     const float2 e = dqt()[k];
