@@ -276,7 +276,9 @@ __device__ __forceinline__ uint32_t find_symbol(const DecArgs &a, float kS, floa
     uint32_t o = o_mu;
     bool far = true, below = true;
     if (w.n + w.w) {
-        const float sigma = __fdividef(1.0f, rs);
+        // sigma for the estimate only: an approximate reciprocal is enough
+        float sigma;
+        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(sigma) : "f"(rs));
         o = estimate<DT>(a, kS, inv_total, s, o_mu, ph_mu, mu, sigma, far, below);
         if (DT == SKV_BF16 && !far) {
             // second pass: p_hat's share and the floor term at the first estimate
@@ -400,10 +402,14 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
             return BITS == 16 ? reinterpret_cast<const uint16_t *>(stage)[at(e)]
                               : reinterpret_cast<const uint8_t *>(stage)[at(e)];
         };
-        // per-symbol inputs of the next symbol, loaded one symbol ahead
+        // per-symbol inputs of the next symbol, loaded one symbol ahead (for
+        // e4m3 its finiteness and order are carried too: 3% faster there, 2%
+        // slower for bf16, whose registers are tighter)
         uint32_t mc_n = get(0);
+        bool fin_n = K::finite(mc_n);
+        uint32_t om_n = K::ord(fin_n ? mc_n : 0u);
         float rs_n = active ? __ldg(rse) : 1.0f;
-        uint32_t ph_n = (active && g.w_h) ? phat_dec<DT, EP>(a, K::ord(K::finite(mc_n) ? mc_n : 0u)) : 0u;
+        uint32_t ph_n = (active && g.w_h) ? phat_dec<DT, EP>(a, om_n) : 0u;
         // One symbol per iteration, unrolled four times: 1% faster than twice;
         // eight times is slower by a quarter (more values live across the body).
 #pragma unroll 4
@@ -424,22 +430,27 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
                 __syncwarp();
             }
             const uint32_t mc = mc_n;
+            const bool fin_c = fin_n;
+            const uint32_t om_c = om_n;
             const float rs = rs_n;
             const uint32_t ph = ph_n;
             if (e + 1u < V && active) {
                 mc_n = get(e + 1u);
+                fin_n = K::finite(mc_n);
+                om_n = K::ord(fin_n ? mc_n : 0u);
                 rs_n = __ldg(rse + e + 1u);
-                if (g.w_h) ph_n = phat_dec<DT, EP>(a, K::ord(K::finite(mc_n) ? mc_n : 0u));
+                if (g.w_h) ph_n = phat_dec<DT, EP>(a, om_n);
             }
             uint32_t slot = 0, o = 0, c = 0, f = 1;
             float mu = 0.0f;
             bool miss = false;
             if (active) {
-                const bool fin = K::finite(mc);
+                const bool fin = DT == SKV_E4M3 ? fin_c : K::finite(mc);
                 bad_mu |= !fin;
                 mu = fin ? K::value(mc) : 0.0f;
                 slot = (uint32_t)x & (M - 1u);
-                o = find_symbol<DT, EP>(a, kS, inv_total, slot, mu, rs, K::ord(fin ? mc : 0u), ph, c, f);
+                o = find_symbol<DT, EP>(a, kS, inv_total, slot, mu, rs, DT == SKV_E4M3 ? om_c : K::ord(fin ? mc : 0u),
+                                        ph, c, f);
                 miss = !(c <= slot && slot - c < f);
             }
             // misses are resolved by the whole warp, one lane at a time
