@@ -275,11 +275,17 @@ __device__ __forceinline__ uint32_t find_symbol(const DecArgs &a, float kS, floa
     const Weights w{a.g.w_n, a.g.w_w, a.g.w_h};
     uint32_t o = o_mu;
     bool far = true, below = true;
+    bool far1 = false;
+    uint32_t o_far = 0;
     if (w.n + w.w) {
         // sigma for the estimate only: an approximate reciprocal is enough
         float sigma;
         asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(sigma) : "f"(rs));
         o = estimate<DT>(a, kS, inv_total, s, o_mu, ph_mu, mu, sigma, far, below);
+        far1 = far;
+        // a lane already far looks its code up now, so that the table load
+        // overlaps the other lanes' second pass
+        if (DT == SKV_BF16 && far1) o_far = saturated_inverse<DT>(a, s, below ? 0u : (w.n + w.w) << 24);
         if (DT == SKV_BF16 && !far) {
             // second pass: p_hat's share and the floor term at the first estimate
             // (bf16 only: e4m3's eight codes per binade leave the first estimate
@@ -289,7 +295,7 @@ __device__ __forceinline__ uint32_t find_symbol(const DecArgs &a, float kS, floa
         }
     }
     // only p_hat holds mass this far out: the saturated inverse gives the code
-    if (far) o = saturated_inverse<DT>(a, s, (below || !(w.n + w.w)) ? 0u : (w.n + w.w) << 24);
+    if (far) o = (DT == SKV_BF16 && far1) ? o_far : saturated_inverse<DT>(a, s, (below || !(w.n + w.w)) ? 0u : (w.n + w.w) << 24);
     const uint32_t clo = cdf_dec<DT, EP>(a, o, mu, rs);
     const uint32_t chi = cdf_dec<DT, EP>(a, o + 1u, mu, rs);
     c_out = clo;
