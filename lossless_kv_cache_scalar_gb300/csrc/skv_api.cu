@@ -587,7 +587,7 @@ static int32_t decode_launch(const Geom &g, const void *bitstream, uint64_t bits
     return launch_decode(da, st) ? SKV_ERR_CUDA : SKV_OK;
 }
 
-static int32_t decode_args_check(const Geom &g, const void *bitstream, const uint64_t *offsets,
+static int32_t decode_args_check(const void *bitstream, const uint64_t *offsets,
                                  const void *mu, const uint32_t *ids, uint64_t n_units, bool pages,
                                  void *out) {
     if (n_units && (!bitstream || !offsets || !mu || !out)) return SKV_ERR_INVALID_ARG;
@@ -607,7 +607,7 @@ static int32_t decode_impl(const skv_layout *lay, const void *bitstream, uint64_
     r = common_checks(g, sigma, counts, status, workspace, ws_bytes, WS_DECODE_MIN);
     if (r != SKV_OK) return r;
     if (!pages) n_units = g.n_chunks;
-    if ((r = decode_args_check(g, bitstream, offsets, mu, ids, n_units, pages, out)) != SKV_OK) return r;
+    if ((r = decode_args_check(bitstream, offsets, mu, ids, n_units, pages, out)) != SKV_OK) return r;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return SKV_ERR_CUDA;
     Workspace ws;
@@ -656,7 +656,7 @@ int32_t skv_decode_chunks_prepared(const skv_layout *lay, const void *bitstream,
     if (r != SKV_OK) return r;
     if (!status || !workspace || ((uintptr_t)workspace & 255u) != 0) return SKV_ERR_INVALID_ARG;
     if (ws_bytes < carve(g, WS_DECODE_MIN, nullptr).bytes) return SKV_ERR_INVALID_ARG;
-    if ((r = decode_args_check(g, bitstream, offsets, mu, chunk_ids, n_ids, true, pages_out)) != SKV_OK)
+    if ((r = decode_args_check(bitstream, offsets, mu, chunk_ids, n_ids, true, pages_out)) != SKV_OK)
         return r;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return SKV_ERR_CUDA;
@@ -758,7 +758,7 @@ int32_t skv_decode_offload(const skv_layout *lay, const void *host_bitstream, ui
     if ((r = common_checks(g, sigma, counts, status, workspace, ws_bytes, WS_DECODE_MIN)) != SKV_OK) return r;
     if (g.n_chunks && (!host_bitstream || !host_offsets || !staging || !aligned16(staging)))
         return SKV_ERR_INVALID_ARG;
-    if ((r = decode_args_check(g, staging, offsets, mu, nullptr, g.n_chunks, false, kv_out)) != SKV_OK)
+    if ((r = decode_args_check(staging, offsets, mu, nullptr, g.n_chunks, false, kv_out)) != SKV_OK)
         return r;
     if (g.n_chunks && (host_offsets[0] != 0 || host_offsets[g.n_chunks] > bitstream_bytes))
         return SKV_ERR_CORRUPT;
@@ -893,7 +893,7 @@ int32_t skv_encode_host(const skv_layout *lay, const void *host_kv, const void *
         const uint32_t l0 = b * lpb, nl = lay->n_layers - l0 < lpb ? lay->n_layers - l0 : lpb;
         const skv_layout sl = sub_layout(lay, nl);
         Geom gs;
-        make_geom(&sl, gs);
+        if (make_geom(&sl, gs) != SKV_OK) return SKV_ERR_INVALID_ARG;   // cannot fail for a valid layout
         const uint64_t kk0 = (uint64_t)l0 * lay->n_kv * g.P;      // the batch's first chunk
         if (cudaStreamWaitEvent(os, encoded.e[h], 0) != cudaSuccess) return SKV_ERR_CUDA;
         if (cudaMemcpyAsync(host_offsets + kk0, hs.offs[h], 8ull * (gs.n_chunks + 1), cudaMemcpyDeviceToHost,
@@ -914,7 +914,7 @@ int32_t skv_encode_host(const skv_layout *lay, const void *host_kv, const void *
         const uint32_t l0 = b * lpb, nl = lay->n_layers - l0 < lpb ? lay->n_layers - l0 : lpb;
         const skv_layout sl = sub_layout(lay, nl);
         Geom gs;
-        make_geom(&sl, gs);
+        if (make_geom(&sl, gs) != SKV_OK) { rc = SKV_ERR_INVALID_ARG; break; }
         const uint64_t e0 = (uint64_t)l0 * lay->n_kv * plane_elems, ne = (uint64_t)nl * lay->n_kv * plane_elems;
         // half h is free once batch b - 2 has been encoded (inputs) and copied out (output)
         if ((b >= 2 && cudaStreamWaitEvent(cs, encoded.e[h], 0) != cudaSuccess) ||
@@ -994,7 +994,7 @@ int32_t skv_decode_host(const skv_layout *lay, const void *host_bits, uint64_t b
         const uint32_t l0 = b * lpb, nl = lay->n_layers - l0 < lpb ? lay->n_layers - l0 : lpb;
         const skv_layout sl = sub_layout(lay, nl);
         Geom gs;
-        make_geom(&sl, gs);
+        if (make_geom(&sl, gs) != SKV_OK) { rc = SKV_ERR_INVALID_ARG; break; }
         const uint64_t k0 = (uint64_t)l0 * lay->n_kv * g.P;
         const uint64_t o0 = host_offsets[k0], nbytes = host_offsets[k0 + gs.n_chunks] - o0;
         const uint64_t e0 = (uint64_t)l0 * lay->n_kv * plane_elems, ne = (uint64_t)nl * lay->n_kv * plane_elems;
