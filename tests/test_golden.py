@@ -54,7 +54,6 @@ def test_mixture_weights_sum_to_one_hundred():
 def test_oracle_tiny_digest():
     from oracle import oracle as O
     from lossless_kv_cache_scalar_gb300 import synth
-    import numpy as np
     g = _load("oracle_tiny.json")
     w = synth.to_numpy(synth.generate(synth.CONFIGS["tiny"]))
     h_in = hashlib.sha256(w["kv"].tobytes() + w["mu"].tobytes() + w["sigma"].tobytes()).hexdigest()
