@@ -22,11 +22,14 @@
  *  - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is the
  *    legacy default stream) and is asynchronous: read outputs and *status
  *    after synchronising that stream.
- *  - The return value reports argument and launch errors found on the host
- *    (SKV_OK, SKV_ERR_INVALID_ARG, SKV_ERR_CUDA); nothing is enqueued when it
- *    is not SKV_OK. Data-dependent errors are written by the device to the
- *    int32 at `status` (device memory), which the call first sets to SKV_OK;
- *    the first error found wins. The device never traps.
+ *  - The return value reports errors found on the host: argument errors
+ *    (SKV_ERR_INVALID_ARG), found before anything is enqueued; launch errors
+ *    (SKV_ERR_CUDA), after which work the call enqueued earlier may still run;
+ *    and, for the calls that read offsets or sizes in host memory, the
+ *    SKV_ERR_CORRUPT or SKV_ERR_CAPACITY results their entries describe.
+ *    Data-dependent errors are written by the device to the int32 at
+ *    `status` (device memory), which the call first sets to SKV_OK; the
+ *    first error found wins. The device never traps.
  *  - Tensor layout is canonical: KV and mu are [n_layers][n_kv][n_tokens]
  *    [n_heads][head_dim] codes, channel fastest, 16-byte aligned; sigma is
  *    float32 [n_layers][n_kv][n_heads][head_dim] (with sigma blocks,
