@@ -138,7 +138,8 @@ int32_t skv_max_encoded_bytes(const skv_layout *lay, uint64_t *bytes);
  *      quantile tables (< 1 MB for these shapes);
  *   2  skv_decode / skv_decode_chunks with the outlier inverse tables as well
  *      (+ 4 * 2^m bytes: 64 MiB for bf16, 256 KiB for e4m3), which make far
- *      outliers cost one lookup instead of a bisection. A decode call uses
+ *      outliers cost one lookup instead of a bisection, and for bf16 the
+ *      512 KiB (edge, P_hat) pair table of the exact test. A decode call uses
  *      these tables whenever ws_bytes is at least this size; the decoded
  *      output is the same either way.
  * The workspace must be 256-byte aligned and not used by another call in flight.
