@@ -362,3 +362,36 @@ def test_full_size_sampled(name):
         assert np.array_equal(got, so), (name, k)
     bits = 8.0 * float(offs_h[-1]) / lay.n_elems
     assert bits < (7.0 if lay.dtype == "bf16" else 4.0), bits
+
+
+def test_concurrent_coders_on_two_streams():
+    """Two Coders (own workspaces, own work counters) encoding and decoding
+    different caches at once on two streams give the serial results: no state
+    is shared between calls beyond what the caller passes."""
+    a = synth.generate(synth.CONFIGS["qwen3_0p6b"].scaled(n_layers=2, n_tokens=1024), "cuda")
+    b = synth.generate(synth.CONFIGS["fp8_32b"].scaled(n_layers=2, n_tokens=600), "cuda")
+    la, lb = H.layout_of(synth.CONFIGS["qwen3_0p6b"].scaled(n_layers=2, n_tokens=1024)), \
+        H.layout_of(synth.CONFIGS["fp8_32b"].scaled(n_layers=2, n_tokens=600))
+    ca, cb = Coder(la), Coder(lb)
+    sa_ref, oa_ref = ca.encode(a["kv"], a["mu"], a["sigma"], a["counts"])
+    sb_ref, ob_ref = cb.encode(b["kv"], b["mu"], b["sigma"], b["counts"])
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outa, offa = ca.alloc_output()
+    outb, offb = cb.alloc_output()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        ca.encode_into(a["kv"], a["mu"], a["sigma"], a["counts"], outa, offa, stream=s1)
+        cb.encode_into(b["kv"], b["mu"], b["sigma"], b["counts"], outb, offb, stream=s2)
+    torch.cuda.synchronize()
+    ca.check_status("a", s1)
+    cb.check_status("b", s2)
+    assert torch.equal(offa, oa_ref) and torch.equal(offb, ob_ref)
+    assert torch.equal(outa[: sa_ref.numel()], sa_ref) and torch.equal(outb[: sb_ref.numel()], sb_ref)
+    ka, kb = torch.empty_like(a["kv"]), torch.empty_like(b["kv"])
+    for _ in range(3):
+        ca.decode_into(sa_ref, oa_ref, a["mu"], a["sigma"], a["counts"], ka, stream=s1)
+        cb.decode_into(sb_ref, ob_ref, b["mu"], b["sigma"], b["counts"], kb, stream=s2)
+    torch.cuda.synchronize()
+    ca.check_status("a", s1)
+    cb.check_status("b", s2)
+    assert torch.equal(ka, a["kv"]) and torch.equal(kb, b["kv"])
