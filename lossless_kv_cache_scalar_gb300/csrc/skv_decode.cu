@@ -185,7 +185,11 @@ template <> __device__ __forceinline__ uint32_t nearest_ord<SKV_E4M3>(float x) {
 // One estimate of the code of slot s, with p_hat's share and the floor term
 // taken at o_ref (ph_ref = P_hat(o_ref)). far: the quantile is within 2^-40 of
 // an end, where only p_hat and the floor hold mass; below: nearer the low end.
-template <uint32_t DT>
+// KEEP_SIDE (the second pass) keeps the first pass's side: taken at mu's own
+// code, the estimate errs away from the centre on the true code's side (p_hat's
+// share and the floor term between mu and the code both push it outwards), so
+// the first pass already picks the true side.
+template <uint32_t DT, bool KEEP_SIDE = false>
 __device__ __forceinline__ uint32_t estimate(const DecArgs &a, float kS, float inv_total,
                                              uint32_t s, uint32_t o_ref, uint32_t ph_ref,
                                              float mu, float sigma, bool &far, bool &below) {
@@ -195,7 +199,7 @@ __device__ __forceinline__ uint32_t estimate(const DecArgs &a, float kS, float i
     const float ph_top = (float)(a.g.w_h << 24) - ph;
     // the quantile of the Gaussian part, measured from whichever end is nearer
     const int d = (int)s - (int)o_ref;
-    below = fmaf((float)d, kS, -ph) <= 0.5f / inv_total;     // the divide is loop-invariant
+    if (!KEEP_SIDE) below = fmaf((float)d, kS, -ph) <= 0.5f / inv_total;     // the divide is loop-invariant
     const int dd = below ? max(d, 0) : max(MN - d, 0);
     const float gt = fmaxf(fmaf((float)dd, kS, below ? -ph : -ph_top) * inv_total, 0.0f);
     far = gt < 9.094947e-13f;                       // 2^-40
@@ -291,7 +295,7 @@ __device__ __forceinline__ uint32_t find_symbol(const DecArgs &a, float kS, floa
             // (bf16 only: e4m3's eight codes per binade leave the first estimate
             // as good as a second one, which measured 14% slower there)
             const uint32_t ph1 = w.h ? phat_dec<DT, EP>(a, o) : 0u;
-            o = estimate<DT>(a, kS, inv_total, s, o, ph1, mu, sigma, far, below);
+            o = estimate<DT, true>(a, kS, inv_total, s, o, ph1, mu, sigma, far, below);
         }
     }
     // only p_hat holds mass this far out: the saturated inverse gives the code
