@@ -46,3 +46,16 @@ def test_model_queries_refuse_host_tensors():
         api.search_eval(lay, counts, q, s, q)
     with pytest.raises(ValueError):
         skv.requantize(torch.zeros(64, dtype=torch.uint8), 64, 4, torch.ones(1), 64)
+
+
+def test_missing_library_raises(monkeypatch):
+    """If the CUDA library cannot be loaded the binding raises: it never
+    substitutes another implementation."""
+    from lossless_kv_cache_scalar_gb300 import _binding as B
+    import os
+    monkeypatch.setattr(B, "_lib", None)
+    monkeypatch.setattr(B, "LIB_PATH", os.path.join(B.HERE, "no_such_library_for_this_test.so"))
+    with pytest.raises(RuntimeError):
+        B.lib()
+    with pytest.raises(RuntimeError):
+        _lay().n_chunks                                # any call that needs the library
