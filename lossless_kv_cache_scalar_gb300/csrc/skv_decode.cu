@@ -211,7 +211,12 @@ __device__ __forceinline__ uint32_t estimate(const DecArgs &a, float kS, float i
     const int k = (int)u;
     const float2 e = dqt()[k];
     const float zt = fmaf(u - (float)k, e.y, e.x);
-    return nearest_ord<DT>(fmaf(below ? zt : -zt, sigma, mu));
+    const float xv = fmaf(below ? zt : -zt, sigma, mu);
+    // bf16's first pass is never the answer (a second pass or the saturated
+    // inverse follows), and any order indexes the tables: no clamp needed
+    if (DT == SKV_BF16 && !KEEP_SIDE)
+        return Codes<SKV_BF16>::ord((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xv)));
+    return nearest_ord<DT>(xv);
 }
 
 // The slow path, run by the whole warp for one lane whose estimate failed.
