@@ -466,7 +466,7 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
                 slot = (uint32_t)x & (M - 1u);
                 o = find_symbol<DT, EP>(a, kS, inv_total, slot, mu, rs, DT == SKV_E4M3 ? om_c : K::ord(fin ? mc : 0u),
                                         ph, c, f);
-                miss = !(c <= slot && slot - c < f);
+                miss = slot - c >= f;    // c, slot < 2^24: c > slot wraps far above any f
             }
             // misses are resolved by the whole warp, one lane at a time
             uint32_t pending = __ballot_sync(0xFFFFFFFFu, miss);
@@ -575,7 +575,7 @@ __global__ void __launch_bounds__(256) search_kernel(const SearchArgs sa) {
         bool miss = false;
         if (active) {
             o = find_symbol<DT, EP>(a, kS, inv_total, slot, mu, rs, o_mu, ph, c, f);
-            miss = !(c <= slot && slot - c < f);
+            miss = slot - c >= f;
         }
         uint32_t pending = __ballot_sync(0xFFFFFFFFu, miss);
         while (pending) {
