@@ -75,7 +75,7 @@ __device__ __forceinline__ void encode_group(const EncArgs &a, const TablesWide 
     const Weights w{g.w_n, g.w_w, g.w_h};
     const uint32_t lt = lanemask_lt();
 
-    int64_t pos = (int64_t)g.cap_words;   // words live in [pos, cap_words)
+    uint32_t pos = (uint32_t)g.cap_words;   // words live in [pos, cap_words)
     uint64_t x = K::L;
     bool bad_mu = false, overflow = false;
 
@@ -118,21 +118,23 @@ __device__ __forceinline__ void encode_group(const EncArgs &a, const TablesWide 
                 const bool emit = active && (x >= ((uint64_t)f << 39));
                 const uint32_t ball = __ballot_sync(0xFFFFFFFFu, emit);
                 if (ball) {
-                    const int cnt = __popc(ball);
-                    if (emit) {
-                        const int64_t idx = pos - cnt + __popc(ball & lt);
-                        if (idx >= 0) slot[idx] = (uint32_t)x;
-                        else overflow = true;
-                        x >>= 32;
+                    const uint32_t cnt = __popc(ball);
+                    // 32-bit word position; cap_words bounds every stream, so running
+                    // out of the slot (flagged) is not expected to happen
+                    if (cnt <= pos) {                  // warp-uniform
+                        if (emit) slot[pos - cnt + __popc(ball & lt)] = (uint32_t)x;
+                        pos -= cnt;
+                    } else {
+                        overflow = true;
                     }
-                    pos -= cnt;
+                    if (emit) x >>= 32;
                 }
                 if (active) x = rans_put<DT>(x, cc[i], f, rf[i]);
             }
         }
     }
     a.states[gid * 32u + lane] = x;
-    if (lane == 0) a.nwords[gid] = pos >= 0 ? (uint32_t)(g.cap_words - pos) : 0u;
+    if (lane == 0) a.nwords[gid] = overflow ? 0u : (uint32_t)(g.cap_words - pos);
     if (__any_sync(0xFFFFFFFFu, bad_mu && nq > 0) && lane == 0) set_status(a.status, SKV_ERR_NONFINITE_MU);
     if (__any_sync(0xFFFFFFFFu, overflow) && lane == 0) set_status(a.status, SKV_ERR_CAPACITY);
 }
