@@ -462,7 +462,7 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
             if (active) {
                 const bool fin = DT == SKV_E4M3 ? fin_c : K::finite(mc);
                 bad_mu |= !fin;
-                mu = fin ? K::value(mc) : 0.0f;
+                mu = fin ? (DT == SKV_E4M3 ? dtab8()->value[mc] : K::value(mc)) : 0.0f;
                 slot = (uint32_t)x & (M - 1u);
                 o = find_symbol<DT, EP>(a, kS, inv_total, slot, mu, rs, DT == SKV_E4M3 ? om_c : K::ord(fin ? mc : 0u),
                                         ph, c, f);

@@ -38,7 +38,7 @@ __device__ __forceinline__ void model8(const TablesWide &tab, const Tables8 &tab
         const uint32_t mc = K::get(muv, e);
         const bool fin = K::finite(mc);
         bad_mu |= !fin;
-        const float mu = fin ? K::value(mc) : 0.0f;
+        const float mu = fin ? (DT == SKV_E4M3 ? tab8.value[mc] : K::value(mc)) : 0.0f;
         const uint32_t o = K::ord(K::get(kvv, e));
         uint32_t c, f;
         if (DT == SKV_BF16) {

@@ -35,6 +35,7 @@ using TablesWide = PhiTables<true>;
 struct Tables8 {         // e4m3 only: the whole alphabet fits on chip
     float edge[257];
     uint32_t phat[257];
+    float value[256];    // value of each code (by bit pattern; NaN codes unused)
 };
 
 struct Weights {
@@ -147,6 +148,7 @@ __device__ void stage_tables(PhiTables<WIDE> &t, Tables8 &t8, const uint32_t *__
             t8.edge[o] = edge_from_values<SKV_E4M3>(o);
             t8.phat[o] = phat[o];
         }
+        for (uint32_t b = threadIdx.x; b < 256u; b += blockDim.x) t8.value[b] = Codes<SKV_E4M3>::value(b);
     }
     __syncthreads();
 }
