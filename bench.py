@@ -32,17 +32,47 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-# Algorithmic 32-bit operations per scalar: the format's own arithmetic for
-# one scalar, counted once. One C(o) is about 45 (edge 9, z 6, narrow Phi 9,
-# wide Phi 11, P_hat 2, mix 3, scale 5); encode = 2 C(o) + ord and mu (6) + the
-# rANS step with renormalisation, ballot placement and the 64/32 division (34);
-# decode = 2 C(o) + slot, update, refill, placement, code and packing (20),
-# search probes beyond the two bracketing edges excluded. e4m3: ord, edges and
-# P_hat on 8-bit codes take 12 fewer per scalar.
-ALG_OPS = {("bf16", "encode"): 130, ("bf16", "decode"): 110,
-           ("e4m3", "encode"): 118, ("e4m3", "decode"): 98}
+# The format's own arithmetic per scalar, by instruction class: the totals
+# table of the SKV v1 format's section 9 (FORMAT.md), read from that file and
+# checked against the library's copy (skv_op_table). The arithmetic roofline
+# is the scalars per second of the matching skv_peak_probe table probe.
+OP_CLASSES = ["fp32", "fminmax", "iadd", "logic", "shift", "iminmax", "imad", "imad_hi", "imad_wide",
+              "cvt", "mufu", "popc", "vote", "lds", "ldt", "sts"]
+OP_TABLES = [("bf16", "encode"), ("bf16", "decode"), ("e4m3", "encode"), ("e4m3", "decode")]
+
+
+def op_tables(check_lib: bool = True) -> dict:
+    """{(dtype, op): {"counts": {class: n}, "instructions": n, "ops": weighted}} from FORMAT.md section 9."""
+    import re
+    out = {}
+    with open(os.path.join(ROOT, "FORMAT.md")) as fh:
+        for line in fh:
+            m = re.match(r"\| (bf16|e4m3) (encode|decode) \|(.*)\|\s*$", line)
+            if not m:
+                continue
+            v = [int(x) for x in m.group(3).split("|")]
+            if len(v) != len(OP_CLASSES) + 2:
+                raise SystemExit(f"FORMAT.md section 9: malformed row {line.strip()}")
+            out[(m.group(1), m.group(2))] = {"counts": dict(zip(OP_CLASSES, v[:-2])), "instructions": v[-2],
+                                             "ops": v[-1]}
+    if sorted(out) != sorted(OP_TABLES):
+        raise SystemExit("FORMAT.md section 9: operation table rows missing")
+    if check_lib:
+        import ctypes as C
+        from lossless_kv_cache_scalar_gb300 import _binding as B
+        n = len(OP_CLASSES)
+        for t, key in enumerate(OP_TABLES):
+            counts, weights = (C.c_uint32 * n)(), (C.c_uint32 * n)()
+            B.check("skv_op_table", B.lib().skv_op_table(t, counts, weights, n))
+            if list(counts) != [out[key]["counts"][c] for c in OP_CLASSES]:
+                raise SystemExit(f"skv_op_table({key}) differs from FORMAT.md section 9")
+            if sum(a * b for a, b in zip(counts, weights)) != out[key]["ops"]:
+                raise SystemExit(f"skv_op_table({key}) weights differ from FORMAT.md section 9")
+    return out
+
+
 SMS = 152               # GB300 streaming multiprocessors
-LANES_PER_SM_CLK = 128  # 4 schedulers x 32 lanes issue per clock
+LANES_PER_SM_CLK = 128  # 4 schedulers x 32 lanes issue per clock (the uniform issue peak, for comparison)
 
 
 def _peaks():
@@ -269,12 +299,14 @@ def main():
     enc_gbs = raw_bytes * args.steps / t_enc / 1e9
     dec_gbs = raw_bytes * args.steps / t_dec / 1e9
 
-    # roofline of the dominant kernel (encode or decode call)
+    # roofline of the dominant kernel (encode or decode call): the format's
+    # operations per scalar (FORMAT.md section 9) over the rate at which the
+    # table probe runs that same operation mix on this GPU
     dom = "decode" if t_dec >= t_enc else "encode"
     t_dom = (t_dec if dom == "decode" else t_enc) / args.steps
     sm_mhz = clocks.get("sm_mhz") or _peaks().get("sm_max_mhz", 2070.0)
-    peak_tops = SMS * LANES_PER_SM_CLK * sm_mhz * 1e6 / 1e12
-    achieved = ALG_OPS[(lay.dtype, dom)] * n_el / t_dom / 1e12
+    uniform_tops = SMS * LANES_PER_SM_CLK * sm_mhz * 1e6 / 1e12
+    tables = op_tables()
     traffic = inst_per_scalar = None
     try:
         with open(args.traffic_json) as fh:
@@ -284,7 +316,18 @@ def main():
     except (OSError, ValueError):
         traffic = None
     hbm_peak = _peaks().get("hbm_gbs", 6685.5)
-    measured_peaks = alu_peaks(dev) if args.alu_probe else None
+    probes = alu_peaks(dev) if args.alu_probe else None
+
+    def arith(op, t_total):
+        """(achieved Tops, peak Tops, frac, frac against the uniform issue peak) for one direction."""
+        tab = tables[(lay.dtype, op)]
+        scal_s = n_el * args.steps / t_total
+        achieved = tab["ops"] * scal_s / 1e12
+        peak = tab["ops"] * probes["tables"][f"{lay.dtype} {op}"] / 1e12 if probes else None
+        return achieved, peak, (achieved / peak if peak else None), achieved / uniform_tops
+
+    a_enc, a_dec = arith("encode", t_enc), arith("decode", t_dec)
+    achieved, peak_tops, frac, frac_uniform = a_dec if dom == "decode" else a_enc
     page_lat = page_latency(coder, out, offsets, w, lay, args, dev) if args.page_latency else None
     inputs = model_inputs_run(w, lay, args, dev, hbm_peak) if args.model_inputs else None
     offload = offload_run(coder, out, offsets, w, lay, args, dev, total_bytes) if args.offload else None
@@ -322,16 +365,23 @@ def main():
             "compression_ratio": 8.0 * lay.bytes_per_code / bits,
             "sigma_side_bits_per_scalar": sigma_side_bits,
             "roofline": {"bound": "alu", "kernel": dom, "achieved": achieved, "peak": peak_tops,
-                         "unit": "Tops/s", "frac": achieved / peak_tops, "traffic": traffic,
-                         "alg_ops_per_scalar": ALG_OPS[(lay.dtype, dom)],
+                         "unit": "Tops/s", "frac": frac, "traffic": traffic,
+                         "alg_ops_per_scalar": tables[(lay.dtype, dom)]["ops"],
+                         "alg_instructions_per_scalar": tables[(lay.dtype, dom)]["instructions"],
                          "ncu_thread_inst_per_scalar": inst_per_scalar,
-                         "peak_basis": f"{SMS} SMs x {LANES_PER_SM_CLK} lane-ops/clk x {sm_mhz:.0f} MHz (sampled)",
+                         "peak_basis": ("measured: skv_peak_probe running the format's %s %s operation table "
+                                        "(FORMAT.md section 9) with full instruction-level parallelism"
+                                        % (lay.dtype, dom)) if probes else "not measured (--alu-probe 0)",
+                         "frac_of_uniform_issue": frac_uniform,
+                         "uniform_issue_tops": uniform_tops,
+                         "uniform_basis": f"{SMS} SMs x {LANES_PER_SM_CLK} lane-ops/clk x {sm_mhz:.0f} MHz (sampled)",
                          "hbm_bound_gbs": hbm_peak * lay.bytes_per_code / (2 * lay.bytes_per_code + bits / 8),
-                         "measured_issue_tops": measured_peaks,
-                         "frac_of_measured_mix": (achieved / measured_peaks["mix"]) if measured_peaks else None,
+                         "probes": probes,
                          "hbm_peak_gbs": hbm_peak},
-            "roofline_encode_frac": ALG_OPS[(lay.dtype, "encode")] * n_el / (t_enc / args.steps) / 1e12 / peak_tops,
-            "roofline_decode_frac": ALG_OPS[(lay.dtype, "decode")] * n_el / (t_dec / args.steps) / 1e12 / peak_tops,
+            "roofline_encode_frac": a_enc[2],
+            "roofline_decode_frac": a_dec[2],
+            "roofline_encode_frac_uniform": a_enc[3],
+            "roofline_decode_frac_uniform": a_dec[3],
             "cpu_baseline": cpu,
             "page_decode_latency_us": page_lat,
             "model_inputs": inputs,
@@ -531,19 +581,18 @@ def requant_run(w, lay, dev, hbm_peak, reps=5, group=128):
 
 
 def alu_peaks(dev, target_ms=20.0):
-    """Issue-rate probes (skv_peak_probe): 32-bit Tops/s for three-input
-    integer add, lop3, integer multiply-add, binary32 multiply and their 1:1:1:1
-    mix, each the best of 3 launches sized to about target_ms."""
+    """skv_peak_probe: the rate of each instruction class of FORMAT.md
+    section 9 alone (Tops/s, 32-bit operations) and of each whole operation
+    table (scalars/s), each the best of 3 launches sized to about target_ms."""
     import ctypes as C
     from lossless_kv_cache_scalar_gb300 import _binding as B
     stream = torch.cuda.Stream(device=dev)
     sink = torch.zeros(1, dtype=torch.int32, device=dev)
-    names = ["iadd3", "lop3", "imad", "fmul", "mix"]
-    out = {}
-    for kind, name in enumerate(names):
-        iters = 64
-        for _ in range(8):                       # grow until a launch takes target_ms
-            ops = C.c_uint64()
+
+    def rate(kind):
+        iters = 16
+        ops = C.c_uint64()
+        for _ in range(10):                      # grow until a launch takes target_ms
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             B.check("skv_peak_probe", B.lib().skv_peak_probe(kind, iters, C.c_void_p(sink.data_ptr()),
@@ -551,7 +600,7 @@ def alu_peaks(dev, target_ms=20.0):
             e1.record(stream)
             stream.synchronize()
             ms = e0.elapsed_time(e1)
-            if ms >= target_ms / 2 or iters >= (1 << 20):
+            if ms >= target_ms / 2 or iters >= (1 << 22):
                 break
             iters = int(iters * max(2.0, target_ms / max(ms, 1e-3)))
         best = 0.0
@@ -562,9 +611,12 @@ def alu_peaks(dev, target_ms=20.0):
                                                              C.byref(ops), C.c_void_p(stream.cuda_stream)))
             e1.record(stream)
             stream.synchronize()
-            best = max(best, ops.value / (e0.elapsed_time(e1) / 1e3) / 1e12)
-        out[name] = best
-    return out
+            best = max(best, ops.value / (e0.elapsed_time(e1) / 1e3))
+        return best
+
+    classes = {name: rate(k) / 1e12 for k, name in enumerate(OP_CLASSES)}
+    tabs = {f"{d} {o}": rate(len(OP_CLASSES) + t) for t, (d, o) in enumerate(OP_TABLES)}
+    return {"class_tops": classes, "tables": tabs, "tables_unit": "scalars/s"}
 
 
 def offload_plan_host(host_offs, batch_bytes, max_chunks):

@@ -403,14 +403,32 @@ int32_t skv_requantize(uint32_t mode, uint32_t b, const void *in, uint64_t n, vo
 /*
  * Measurement aid (the pages describe no such call): one launch of an
  * arithmetic issue-rate probe, for the arithmetic roofline of the coder's
- * kernels. kind: 0 three-input integer add, 1 three-input logic (lop3),
- * 2 integer multiply-add, 3 binary32 multiply, 4 the four in turn. Every SM
- * runs 8 CTAs of 256 threads, each thread 8 independent chains for
- * iters x 16 steps. *ops receives the 32-bit operations the launch issues
- * (host, at once); time the launch on `stream` (CUDA events) to get the rate.
+ * kernels. kind 0..15: one instruction class of the operation count in the
+ * SKV v1 format's section 9 (0 binary32 add/mul/fma, 1 binary32 min/max,
+ * 2 integer add, 3 logic (lop3), 4 shift, 5 integer min/max, 6 integer
+ * multiply-add, 7 multiply-high, 8 32x32->64 multiply, 9 float/integer
+ * conversion, 10 rcp/lg2 approximation, 11 popc, 12 ballot (with its setp),
+ * 13 shared-memory load, 14 L1-resident global load, 15 shared-memory store);
+ * *ops receives the launch's 32-bit operations (the class's weight per
+ * instruction). kind 16..19: the whole operation table of bf16 encode, bf16
+ * decode, e4m3 encode, e4m3 decode, issued with full instruction-level
+ * parallelism; *ops receives the scalars modelled (each scalar's operations
+ * are the table's counts). Every SM runs 8 CTAs of 256 threads, each thread
+ * 8 independent chains. *ops is written on the host at once; time the launch
+ * on `stream` (CUDA events) for the rate.
  * sink: device uint32, written only if the chains hit one unlikely value.
  */
 int32_t skv_peak_probe(int32_t kind, uint32_t iters, uint32_t *sink, uint64_t *ops, void *stream);
+
+/*
+ * The operation count of the SKV v1 format's section 9 as this library holds
+ * it (the pages describe no such table; it defines the arithmetic roofline).
+ * table: 0 bf16 encode, 1 bf16 decode, 2 e4m3 encode, 3 e4m3 decode.
+ * counts[c] receives the instructions of class c per scalar and weights[c]
+ * its 32-bit operations per instruction, for the n = 16 classes of
+ * skv_peak_probe. Host only, no device work; INVALID_ARG for another n.
+ */
+int32_t skv_op_table(int32_t table, uint32_t *counts, uint32_t *weights, uint32_t n);
 
 /*
  * The decoder's slot-to-code search on its own, for exhaustive checks: query

@@ -55,6 +55,7 @@ SIGNATURES = {
     "skv_decode_host": (_i32, [_LP, _vp, _u64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _u64, _u32, _vp, _vp, _vp]),
     "skv_search_eval": (_i32, [_LP, _vp, _u64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _u64, _vp]),
     "skv_peak_probe": (_i32, [_i32, _u32, _vp, C.POINTER(_u64), _vp]),
+    "skv_op_table": (_i32, [_i32, C.POINTER(_u32), C.POINTER(_u32), _u32]),
     "skv_decode_pages_host": (_i32, [_LP, _vp, _u64, _vp, _vp, _vp, _u32, _vp, _vp, _vp, _u64, _vp, _u64, _vp,
                                      _vp]),
     "skv_offload_plan": (_i32, [_vp, _u64, _u64, _u64, _vp, _u64, C.POINTER(_u64)]),

@@ -9,6 +9,7 @@
 #include <vector>
 
 #include "skv_model.cuh"
+#include "skv_ops.h"
 
 namespace skv {
 
@@ -24,6 +25,7 @@ int launch_requantize(uint32_t mode, uint32_t b, const void *in, uint64_t n, voi
                       float *s_out, uint64_t n_groups, cudaStream_t st);
 int launch_peak(int kind, uint32_t iters, uint32_t *sink, uint32_t blocks, cudaStream_t st);
 uint64_t peak_ops(int kind, uint32_t iters, uint32_t blocks);
+int num_probe_kinds();
 int launch_search_eval(const SearchArgs &sa, cudaStream_t st);
 int launch_search_aids(const Geom &g, const uint32_t *phat, float *qt, uint16_t *inv_lo,
                        uint16_t *inv_hi, cudaStream_t st);
@@ -834,7 +836,7 @@ int32_t skv_requantize(uint32_t mode, uint32_t b, const void *in, uint64_t n, vo
 }
 
 int32_t skv_peak_probe(int32_t kind, uint32_t iters, uint32_t *sink, uint64_t *ops, void *stream) {
-    if (kind < 0 || kind > 4 || iters == 0 || !sink || !ops) return SKV_ERR_INVALID_ARG;
+    if (kind < 0 || kind >= num_probe_kinds() || iters == 0 || !sink || !ops) return SKV_ERR_INVALID_ARG;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -842,6 +844,16 @@ int32_t skv_peak_probe(int32_t kind, uint32_t iters, uint32_t *sink, uint64_t *o
     const uint32_t blocks = (uint32_t)sms * 8u;
     *ops = peak_ops(kind, iters, blocks);
     return launch_peak(kind, iters, sink, blocks, static_cast<cudaStream_t>(stream)) ? SKV_ERR_CUDA : SKV_OK;
+}
+
+int32_t skv_op_table(int32_t table, uint32_t *counts, uint32_t *weights, uint32_t n) {
+    if (table < 0 || table >= kNumOpTables || n != (uint32_t)kNumOpClasses || !counts || !weights)
+        return SKV_ERR_INVALID_ARG;
+    for (int c = 0; c < kNumOpClasses; ++c) {
+        counts[c] = kOpCount[table][c];
+        weights[c] = kOpWeight[c];
+    }
+    return SKV_OK;
 }
 
 int32_t skv_host_staging_bytes(const skv_layout *lay, uint32_t layers_per_batch, int32_t op,

@@ -154,35 +154,59 @@ __device__ void stage_tables(PhiTables<WIDE> &t, Tables8 &t8, const uint32_t *__
 }
 
 // -------------------------------------------------------------- model: C(o)
+//
+// C(o) of FORMAT.md section 5 in a form that keeps most steps on the binary32
+// pipe, each step exact:
+//  - zq = floor(z 2^16): one multiply-add rounded down, z 2^16 + 1.5 2^23,
+//    whose exact value lies in [2^23, 2^24) where binary32 spacing is 1, so the
+//    rounding is the floor and the result's bit pattern is kMagicBits + zq;
+//  - zw = floor(zq / 3): (zq + 3 2^19) is exact in binary32 (an integer below
+//    2^22), and its product with the binary32 value just above 1/3 exceeds the
+//    true quotient by less than 0.032, which never crosses the next integer
+//    (the quotient's fraction is 0, 1/3 or 2/3), so a second multiply-add
+//    rounded down gives floor((zq + 3 2^19) / 3) = zw + 2^19 in its bits;
+//  - Phi_q's table position j and remainder r come from the biased bits
+//    directly (the bias is a multiple of 256);
+//  - floor(S (M - N) / 2^24) = hi32(2S (M - N) 2^7), then / 100 by the
+//    multiply-high with ceil(2^37 / 100), exact for every 32-bit dividend.
+// Every identity is exact over the whole range the format allows, so C(o) is
+// bit-identical to the section 5 formula.
 
-// Phi_q(zq) (FORMAT.md section 3) for zq in the table's range: [-2^19, 2^19],
-// or for the wide table [-3 2^19, 3 2^19].
+constexpr uint32_t kMagicBits = 0x4B400000u;     // bits of 1.5 2^23: bits = kMagicBits + integer part
+
+// Phi_q at the grid position k held as b = bias + k (bias a multiple of 2^8).
 template <bool WIDE>
-__device__ __forceinline__ uint32_t phi_q(const PhiTables<WIDE> &t, int zq) {
-    const uint2 e = t.phi[(zq >> 8) + PhiTables<WIDE>::kCenter];
-    return e.x + ((e.y * (uint32_t)(zq & 255)) >> 8);
+__device__ __forceinline__ uint32_t phi_b(const PhiTables<WIDE> &t, uint32_t b, uint32_t bias) {
+    const uint2 e = t.phi[(int)(b >> 8) - (int)(bias >> 8) + PhiTables<WIDE>::kCenter];
+    return e.x + ((e.y * (b & 255u)) >> 8);
 }
 
-// C(o) for an element with predictor value mu and rs = fl32(1/sigma).
+// C(o) for an element with predictor value mu and rs = fl32(1/sigma), from
+// the edge E = E(o) and P_hat(o).
+template <uint32_t DT, bool WIDE>
+__device__ __forceinline__ uint32_t cdf_from(const PhiTables<WIDE> &t, const Weights w, float E, uint32_t ph,
+                                             uint32_t o, float mu, float rs) {
+    constexpr uint32_t MN = (1u << Codes<DT>::m) - Codes<DT>::N;
+    float z = __fmul_rn(__fsub_rn(E, mu), rs);
+    z = fminf(fmaxf(z, -24.0f), 24.0f);
+    const float tq = __fmaf_rd(z, 65536.0f, 12582912.0f);          // bits: kMagicBits + zq
+    const uint32_t bq = __float_as_uint(tq);
+    const uint32_t bn = WIDE ? bq : min(max(bq, kMagicBits - 524288u), kMagicBits + 524288u);
+    // bits: kMagicBits + 2^19 + zw
+    const uint32_t bw = __float_as_uint(__fmaf_rd(__fadd_rn(tq, -11010048.0f), 0.333333343f, 12582912.0f));
+    // 2S (< 2^32): the weights doubled
+    const uint32_t S2 = (2u * w.n) * phi_b(t, bn, kMagicBits) + (2u * w.w) * phi_b(t, bw, kMagicBits + 524288u) +
+                        (2u * w.h) * ph;
+    return o + (__umulhi(__umulhi(S2, MN << 7), 0x51EB851Fu) >> 5);
+}
+
+// C(o) with the edge and P_hat from the code's own tables.
 template <uint32_t DT, bool WIDE>
 __device__ __forceinline__ uint32_t cdf(const PhiTables<WIDE> &t, const Tables8 *t8, const Weights w,
                                         const uint32_t *__restrict__ phat, uint32_t o, float mu,
                                         float rs) {
     using K = Codes<DT>;
-    constexpr uint32_t MN = (1u << K::m) - K::N;
-    const float E = K::edge(t8, o);
-    const float d = __fsub_rn(E, mu);
-    float z = __fmul_rn(d, rs);
-    z = fminf(fmaxf(z, -24.0f), 24.0f);
-    const int zq = __float2int_rd(__fmul_rn(z, 65536.0f));
-    const int zn = WIDE ? zq : max(min(zq, 524288), -524288);
-    // floor(zq / 3) for zq in [-3 * 2^19, 3 * 2^19]
-    const int zw = (int)(__umulhi((uint32_t)(zq + 1572864), 0xAAAAAAABu) >> 1) - 524288;
-    // branch-free: a zero weight multiplies its term away (P_hat is all zeros
-    // when its weight is 0), so one straight-line block serves every mixture
-    const uint32_t S = w.n * phi_q(t, zn) + w.w * phi_q(t, zw) + w.h * K::phat(t8, phat, o);
-    const uint64_t prod = (uint64_t)S * MN;
-    return o + (uint32_t)(prod >> 24) / 100u;
+    return cdf_from<DT>(t, w, K::edge(t8, o), K::phat(t8, phat, o), o, mu, rs);
 }
 
 // C(o) as cdf<SKV_BF16>, with the edge E(o) and P_hat(o) read as one pair
@@ -193,17 +217,8 @@ template <bool WIDE>
 __device__ __forceinline__ uint32_t cdf_ep(const PhiTables<WIDE> &t, const Weights w,
                                            const uint2 *__restrict__ ep, uint32_t o, float mu,
                                            float rs) {
-    constexpr uint32_t MN = (1u << 24) - 65536u;
     const uint2 e = __ldg(ep + o);
-    const float d = __fsub_rn(__uint_as_float(e.x), mu);
-    float z = __fmul_rn(d, rs);
-    z = fminf(fmaxf(z, -24.0f), 24.0f);
-    const int zq = __float2int_rd(__fmul_rn(z, 65536.0f));
-    const int zn = WIDE ? zq : max(min(zq, 524288), -524288);
-    const int zw = (int)(__umulhi((uint32_t)(zq + 1572864), 0xAAAAAAABu) >> 1) - 524288;
-    const uint32_t S = w.n * phi_q(t, zn) + w.w * phi_q(t, zw) + w.h * e.y;
-    const uint64_t prod = (uint64_t)S * MN;
-    return o + (uint32_t)(prod >> 24) / 100u;
+    return cdf_from<SKV_BF16>(t, w, __uint_as_float(e.x), e.y, o, mu, rs);
 }
 
 // ------------------------------------------------------------------- rANS
