@@ -26,6 +26,8 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "skv_model.cuh"
 
 namespace skv {
@@ -38,9 +40,8 @@ template <uint32_t DT> struct DecShape { static constexpr int warps = 32, ctas =
 static_assert(DecShape<SKV_BF16>::warps * DecShape<SKV_BF16>::ctas == (int)kDecResidentWarps &&
               DecShape<SKV_E4M3>::warps * DecShape<SKV_E4M3>::ctas == (int)kDecResidentWarps,
               "decoder residency");
-constexpr uint32_t kRing = 256;        // words per warp ring
-constexpr uint32_t kBlock = 64;        // words per cp.async batch (16 B per lane, 16 lanes)
-constexpr uint32_t kStepSyms = 4;      // the ring is topped up every 4 symbols
+constexpr uint32_t kRing = 256;        // words per warp ring: 4 blocks
+constexpr uint32_t kBlock = 64;        // words per cp.async block (16 B per lane, 16 lanes)
 // per warp: the word ring, then a 512-byte stage holding each lane's 16-byte
 // vector of mu codes, transposed ([word][lane]) so lanes hit distinct banks;
 // decoded codes overwrite their mu codes in place
@@ -185,38 +186,58 @@ template <> __device__ __forceinline__ uint32_t nearest_ord<SKV_E4M3>(float x) {
 // One estimate of the code of slot s, with p_hat's share and the floor term
 // taken at o_ref (ph_ref = P_hat(o_ref)). far: the quantile is within 2^-40 of
 // an end, where only p_hat and the floor hold mass; below: nearer the low end.
-// KEEP_SIDE (the second pass) keeps the first pass's side: taken at mu's own
-// code, the estimate errs away from the centre on the true code's side (p_hat's
-// share and the floor term between mu and the code both push it outwards), so
-// the first pass already picks the true side.
-template <uint32_t DT, bool KEEP_SIDE = false>
-__device__ __forceinline__ uint32_t estimate(const DecArgs &a, float kS, float inv_total,
-                                             uint32_t s, uint32_t o_ref, uint32_t ph_ref,
-                                             float mu, float sigma, bool &far, bool &below) {
+// Besides the code's order it keeps what a second pass reuses: the quantile gt,
+// its log2, the table's z there and the table cell's slope.
+struct Estimate {
+    uint32_t o;
+    float gt, lg, zt, dz;
+    bool far, below;
+};
+template <uint32_t DT>
+__device__ __forceinline__ Estimate estimate(const DecArgs &a, float kS, float inv_total, uint32_t s,
+                                             uint32_t o_ref, uint32_t ph_ref, float mu, float sigma) {
     using K = Codes<DT>;
     constexpr int MN = (int)((1u << K::m) - K::N);
+    Estimate r;
     const float ph = (float)(a.g.w_h * ph_ref);
     const float ph_top = (float)(a.g.w_h << 24) - ph;
     // the quantile of the Gaussian part, measured from whichever end is nearer
     const int d = (int)s - (int)o_ref;
-    if (!KEEP_SIDE) below = fmaf((float)d, kS, -ph) <= 0.5f / inv_total;     // the divide is loop-invariant
-    const int dd = below ? max(d, 0) : max(MN - d, 0);
-    const float gt = fmaxf(fmaf((float)dd, kS, below ? -ph : -ph_top) * inv_total, 0.0f);
-    far = gt < 9.094947e-13f;                       // 2^-40
+    r.below = fmaf((float)d, kS, -ph) <= 0.5f / inv_total;     // the divide is loop-invariant
+    const int dd = r.below ? d : MN - d;
+    // a negative dd (the slot below the reference's p_hat and floor mass) is far
+    r.gt = fmaf((float)dd, kS, r.below ? -ph : -ph_top) * inv_total;
+    r.far = !(r.gt >= 9.094947e-13f);                   // 2^-40
     // an estimate only: lg2 without subnormal handling (a subnormal gt is far)
-    float lg;
-    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(gt));
-    const float u = fminf(fmaxf(fmaf(-lg, (float)kQuantSteps, -(float)kQuantSteps), 0.0f),
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(r.lg) : "f"(r.gt));
+    const float u = fminf(fmaxf(fmaf(-r.lg, (float)kQuantSteps, -(float)kQuantSteps), 0.0f),
                           (float)kQuantN - 0.001f);
     const int k = (int)u;
     const float2 e = dqt()[k];
-    const float zt = fmaf(u - (float)k, e.y, e.x);
-    const float xv = fmaf(below ? zt : -zt, sigma, mu);
+    r.zt = fmaf(u - (float)k, e.y, e.x);
+    r.dz = e.y * (float)kQuantSteps;
+    const float xv = fmaf(r.below ? r.zt : -r.zt, sigma, mu);
     // bf16's first pass is never the answer (a second pass or the saturated
     // inverse follows), and any order indexes the tables: no clamp needed
-    if (DT == SKV_BF16 && !KEEP_SIDE)
-        return Codes<SKV_BF16>::ord((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xv)));
-    return nearest_ord<DT>(xv);
+    if (DT == SKV_BF16) r.o = Codes<SKV_BF16>::ord((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xv)));
+    else r.o = nearest_ord<DT>(xv);
+    return r;
+}
+
+// The second pass (bf16): p_hat's share and the floor term retaken at the
+// first estimate o1 move the quantile by D; the new quantile's log2 moves z
+// along the first pass's table cell (taken at mu's code, the first estimate
+// errs outwards on the true code's side, so its side is kept).
+__device__ __forceinline__ uint32_t estimate2(const DecArgs &a, float kS, float inv_total, const Estimate &e1,
+                                              uint32_t o_ref, uint32_t ph_ref, uint32_t o1, uint32_t ph1,
+                                              float mu, float sigma, bool &far) {
+    const float D = fmaf((float)(int)(o1 - o_ref), kS, (float)((int)a.g.w_h * (int)(ph1 - ph_ref)));
+    const float gt = fmaf(e1.below ? -D : D, inv_total, e1.gt);
+    far = !(gt >= 9.094947e-13f);
+    float lg;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(gt));
+    const float zt = fmaf(e1.dz, e1.lg - lg, e1.zt);
+    return nearest_ord<SKV_BF16>(fmaf(e1.below ? zt : -zt, sigma, mu));
 }
 
 // The slow path, run by the whole warp for one lane whose estimate failed.
@@ -284,27 +305,32 @@ __device__ __forceinline__ uint32_t find_symbol(const DecArgs &a, float kS, floa
     const Weights w{a.g.w_n, a.g.w_w, a.g.w_h};
     uint32_t o = o_mu;
     bool far = true, below = true;
-    bool far1 = false;
-    uint32_t o_far = 0;
     if (w.n + w.w) {
         // sigma for the estimate only: an approximate reciprocal is enough
         float sigma;
         asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(sigma) : "f"(rs));
-        o = estimate<DT>(a, kS, inv_total, s, o_mu, ph_mu, mu, sigma, far, below);
-        far1 = far;
+        const Estimate e1 = estimate<DT>(a, kS, inv_total, s, o_mu, ph_mu, mu, sigma);
+        o = e1.o;
+        far = e1.far;
+        below = e1.below;
+        uint32_t o_far = 0;
         // a lane already far looks its code up now, so that the table load
         // overlaps the other lanes' second pass
-        if (DT == SKV_BF16 && far1) o_far = saturated_inverse<DT>(a, s, below ? 0u : (w.n + w.w) << 24);
+        if (DT == SKV_BF16 && far) o_far = saturated_inverse<DT>(a, s, below ? 0u : (w.n + w.w) << 24);
         if (DT == SKV_BF16 && !far) {
-            // second pass: p_hat's share and the floor term at the first estimate
-            // (bf16 only: e4m3's eight codes per binade leave the first estimate
-            // as good as a second one, which measured 14% slower there)
+            // second pass (bf16 only: e4m3's eight codes per binade leave the
+            // first estimate as good as a second one)
             const uint32_t ph1 = w.h ? phat_dec<DT, EP>(a, o) : 0u;
-            o = estimate<DT, true>(a, kS, inv_total, s, o, ph1, mu, sigma, far, below);
+            o = estimate2(a, kS, inv_total, e1, o_mu, ph_mu, o, ph1, mu, sigma, far);
+            // only p_hat holds mass this far out: the saturated inverse gives the code
+            if (far) o = saturated_inverse<DT>(a, s, below ? 0u : (w.n + w.w) << 24);
+        } else if (far) {
+            o = DT == SKV_BF16 ? o_far : saturated_inverse<DT>(a, s, below ? 0u : (w.n + w.w) << 24);
         }
+    } else {
+        // p_hat alone: the saturated inverse is the answer
+        o = saturated_inverse<DT>(a, s, 0u);
     }
-    // only p_hat holds mass this far out: the saturated inverse gives the code
-    if (far) o = (DT == SKV_BF16 && far1) ? o_far : saturated_inverse<DT>(a, s, (below || !(w.n + w.w)) ? 0u : (w.n + w.w) << 24);
     const uint32_t clo = cdf_dec<DT, EP>(a, o, mu, rs);
     const uint32_t chi = cdf_dec<DT, EP>(a, o + 1u, mu, rs);
     c_out = clo;
@@ -320,7 +346,7 @@ __device__ __forceinline__ void cp_async16(uint32_t *smem, const uint32_t *gmem)
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait2() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
 
 // Decode one group of 32 streams (gid = chunk unit * G + group) with this warp.
 template <uint32_t DT, bool EP>
@@ -379,128 +405,146 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
         return;
     }
 
-    const int64_t nq = (int64_t)stream_vectors(g, cs.n_vec, s);
-    const int64_t nq0 = (int64_t)stream_vectors(g, cs.n_vec, grp * 32u);
-    const uint8_t *mup = a.mu + cs.elem0 * K::bytes;
-    const float *rsp = a.rsig + sigma_row(g, k) * g.HD;
-    uint8_t *outp = a.ids ? a.out + unit * a.page_elems * K::bytes : a.out + cs.elem0 * K::bytes;
+    const uint64_t nq = stream_vectors(g, cs.n_vec, s);
+    const uint64_t nq0 = stream_vectors(g, cs.n_vec, grp * 32u);
+    // the lane's vectors q = s + j W: their mu and output, by pointer steps of W vectors
+    const uint4 *mvp = reinterpret_cast<const uint4 *>(a.mu + cs.elem0 * K::bytes) + s;
+    uint4 *ovp = reinterpret_cast<uint4 *>(a.ids ? a.out + unit * a.page_elems * K::bytes
+                                                 : a.out + cs.elem0 * K::bytes) + s;
+    // sigma row of the chunk and the channel of the lane's vector (advanced by W V mod HD)
+    const float *rsrow = a.rsig + sigma_row(g, k) * g.HD;
+    uint32_t ch = (uint32_t)(((uint64_t)s * V) % g.HD);
+    const uint32_t chstep = (uint32_t)(((uint64_t)g.W * V) % g.HD);
     const float kS = (float)(100.0 * 16777216.0 / (double)((1u << m) - K::N));
     const float inv_total = (g.w_n + g.w_w) ? 1.0f / ((float)(g.w_n + g.w_w) * 16777216.0f) : 0.0f;
     const uint32_t lt = lanemask_lt();
     bool bad_mu = false;
 
+    // The word ring: 4 blocks of 64 words. Block b sits at ring[(64 b) mod 256];
+    // when the read pointer enters block b, block b + 3 is requested and the
+    // wait leaves only the two newest requests (b + 2, b + 3) in flight, so
+    // blocks b and b + 1 have landed (one step reads at most 32 words).
+    auto request = [&](uint32_t blk) {
+        const uint32_t w0 = blk * kBlock + 4u * lane;
+        if (lane < kBlock / 4 && w0 < nwp4) cp_async16(ring + (w0 & (kRing - 1)), words + w0);
+        cp_async_commit();
+    };
+    request(0);
+    request(1);
+    request(2);
+    request(3);
+    cp_async_wait2();
+    __syncwarp();
     uint32_t rp = 0;        // next word to consume (warp-uniform)
-    uint32_t filled = 0;    // words requested into the ring so far (warp-uniform)
-
 
     uint32_t *stage = ring + kRing;              // [4 words][32 lanes]
-    for (int64_t j = 0; j < nq0; ++j) {
-        const bool active = j < nq;
-        const uint64_t q = s + (uint64_t)j * g.W;
-        const float *rse = rsp + (uint32_t)((q * V) % g.HD);
+    // One vector of every lane's stream. TAIL: the group's last vector, which
+    // the streams past the chunk's end (the higher lanes) do not have.
+    auto vector = [&](auto tail, uint64_t j) {
+        constexpr bool TAIL = decltype(tail)::value;
+        const bool active = !TAIL || j < nq;
         // mu of this vector into the lane's stage column; the next vector is
         // only prefetched into L2
-        {
-            const uint4 muv = active ? __ldg(reinterpret_cast<const uint4 *>(mup) + q) : make_uint4(0, 0, 0, 0);
-            stage[0 * 32 + lane] = muv.x;
-            stage[1 * 32 + lane] = muv.y;
-            stage[2 * 32 + lane] = muv.z;
-            stage[3 * 32 + lane] = muv.w;
+        uint4 muv = make_uint4(0, 0, 0, 0);
+        if (active) {
+            asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(muv.x), "=r"(muv.y), "=r"(muv.z), "=r"(muv.w) : "l"(mvp));
         }
-        if (j + 1 < nq) asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const uint4 *>(mup) + q + g.W));
-        // code e of the lane's vector in the stage: word e / (32 / BITS), part e mod (32 / BITS)
-        auto at = [&](uint32_t e) -> uint32_t {
-            constexpr uint32_t per = 32u / BITS;
-            return ((e / per) * 32u + lane) * per + (e % per);
-        };
-        auto get = [&](uint32_t e) -> uint32_t {
-            return BITS == 16 ? reinterpret_cast<const uint16_t *>(stage)[at(e)]
-                              : reinterpret_cast<const uint8_t *>(stage)[at(e)];
-        };
-        // per-symbol inputs of the next symbol, loaded one symbol ahead (for
-        // e4m3 its finiteness and order are carried too: 3% faster there, 2%
-        // slower for bf16, whose registers are tighter)
-        uint32_t mc_n = get(0);
-        bool fin_n = K::finite(mc_n);
-        uint32_t om_n = K::ord(fin_n ? mc_n : 0u);
-        float rs_n = active ? __ldg(rse) : 1.0f;
-        uint32_t ph_n = (active && g.w_h) ? phat_dec<DT, EP>(a, om_n) : 0u;
-        // One symbol per iteration, unrolled four times: 1% faster than twice;
-        // eight times is slower by a quarter (more values live across the body).
-#pragma unroll 4
-        for (uint32_t e = 0; e < V; ++e) {
-            if ((e & (kStepSyms - 1u)) == 0u) {
-                // Keep the ring ahead of the reader: 4 symbols use at most 128 words.
-                const uint32_t need = min(nw, rp + 32u * kStepSyms);
-                const uint32_t target = min(nwp4, rp + 32u * kStepSyms + kBlock);
-                bool issued_extra = false;
-                while (filled < target) {
-                    const uint32_t w0 = filled + 4u * lane;
-                    if (lane < kBlock / 4 && w0 < nwp4) cp_async16(ring + (w0 & (kRing - 1)), words + w0);
-                    cp_async_commit();
-                    issued_extra = filled >= need;
-                    filled += kBlock;
+        if (j + 1 < nq) asm volatile("prefetch.global.L2 [%0];" ::"l"(mvp + g.W));
+        stage[0 * 32 + lane] = muv.x;
+        stage[1 * 32 + lane] = muv.y;
+        stage[2 * 32 + lane] = muv.z;
+        stage[3 * 32 + lane] = muv.w;
+        {
+            // a non-finite mu code anywhere in the vector (rare): report it and
+            // model those elements with mu = +0 (FORMAT.md section 4). A part of
+            // t is zero exactly where a code's exponent field is all ones.
+            constexpr uint32_t E = BITS == 16 ? 0x7F807F80u : 0x7F7F7F7Fu;
+            constexpr uint32_t ONE = BITS == 16 ? 0x00010001u : 0x01010101u;
+            constexpr uint32_t TOP = BITS == 16 ? 0x80008000u : 0x80808080u;
+            auto nonfinite = [&](uint32_t w) { const uint32_t t = (w & E) ^ E; return (t - ONE) & ~t & TOP; };
+            const uint32_t nf = nonfinite(muv.x) | nonfinite(muv.y) | nonfinite(muv.z) | nonfinite(muv.w);
+            if (__any_sync(0xFFFFFFFFu, nf != 0u)) {
+#pragma unroll 1
+                for (uint32_t e = 0; e < V; ++e) {
+                    const uint32_t i = ((e / (32u / BITS)) * 32u + lane) * (32u / BITS) + e % (32u / BITS);
+                    const uint32_t c = BITS == 16 ? (uint32_t)reinterpret_cast<uint16_t *>(stage)[i]
+                                                  : (uint32_t)reinterpret_cast<uint8_t *>(stage)[i];
+                    if (!K::finite(c)) {
+                        bad_mu = true;
+                        if (BITS == 16) reinterpret_cast<uint16_t *>(stage)[i] = 0;
+                        else reinterpret_cast<uint8_t *>(stage)[i] = 0;
+                    }
                 }
-                if (issued_extra) cp_async_wait1(); else cp_async_wait0();
                 __syncwarp();
             }
-            const uint32_t mc = mc_n;
-            const bool fin_c = fin_n;
-            const uint32_t om_c = om_n;
-            const float rs = rs_n;
-            const uint32_t ph = ph_n;
-            if (e + 1u < V && active) {
-                mc_n = get(e + 1u);
-                fin_n = K::finite(mc_n);
-                om_n = K::ord(fin_n ? mc_n : 0u);
-                rs_n = __ldg(rse + e + 1u);
-                if (g.w_h) ph_n = phat_dec<DT, EP>(a, om_n);
-            }
-            uint32_t slot = 0, o = 0, c = 0, f = 1;
-            float mu = 0.0f;
-            bool miss = false;
-            if (active) {
-                const bool fin = DT == SKV_E4M3 ? fin_c : K::finite(mc);
-                bad_mu |= !fin;
-                mu = fin ? (DT == SKV_E4M3 ? dtab8()->value[mc] : K::value(mc)) : 0.0f;
-                slot = (uint32_t)x & (M - 1u);
-                o = find_symbol<DT, EP>(a, kS, inv_total, slot, mu, rs, DT == SKV_E4M3 ? om_c : K::ord(fin ? mc : 0u),
-                                        ph, c, f);
-                miss = slot - c >= f;    // c, slot < 2^24: c > slot wraps far above any f
-            }
-            // misses are resolved by the whole warp, one lane at a time
-            uint32_t pending = __ballot_sync(0xFFFFFFFFu, miss);
-            while (pending) {
-                const uint32_t Lm = __ffs(pending) - 1u;
-                pending &= pending - 1u;
-                cooperative_search<DT, EP>(a, Lm, slot, mu, rs, o, c, c + f, o, c, f);
-            }
-            if (active) {
-                x = (uint64_t)f * (x >> m) + slot - c;
-                // the decoded code replaces its (already read) mu code
-                if (BITS == 16) reinterpret_cast<uint16_t *>(stage)[at(e)] = (uint16_t)K::code(o);
-                else reinterpret_cast<uint8_t *>(stage)[at(e)] = (uint8_t)K::code(o);
-            }
-            const bool refill = active && x < L;
-            const uint32_t ball = __ballot_sync(0xFFFFFFFFu, refill);
-            if (ball) {
-                if (refill) {
-                    const uint32_t idx = rp + __popc(ball & lt);
-                    uint32_t wd = 0;
-                    if (idx < nw) wd = ring[idx & (kRing - 1)];
-                    else corrupt = true;
-                    x = (x << 32) | wd;
+        }
+        const float *rse = rsrow + ch;
+        ch += chstep;
+        if (ch >= g.HD) ch -= g.HD;
+        // the lane's codes: word w of the vector at stage[32 w + lane], PER codes a word
+        constexpr uint32_t PER = 32u / BITS;
+#pragma unroll 1
+        for (uint32_t wi = 0; wi < 4u; ++wi, rse += PER) {
+            uint32_t *sw = stage + wi * 32u + lane;
+#pragma unroll
+            for (uint32_t pi = 0; pi < PER; ++pi) {
+                uint32_t slot = 0, o = 0, c = 0, f = 1;
+                float mu = 0.0f, rs = 1.0f;
+                bool miss = false;
+                if (active) {
+                    const uint32_t mc = BITS == 16 ? (uint32_t)reinterpret_cast<const uint16_t *>(sw)[pi]
+                                                   : (uint32_t)reinterpret_cast<const uint8_t *>(sw)[pi];
+                    mu = DT == SKV_E4M3 ? dtab8()->value[mc] : K::value(mc);
+                    rs = __ldg(rse + pi);
+                    const uint32_t om = K::ord(mc);
+                    const uint32_t ph = g.w_h ? phat_dec<DT, EP>(a, om) : 0u;
+                    slot = (uint32_t)x & (M - 1u);
+                    o = find_symbol<DT, EP>(a, kS, inv_total, slot, mu, rs, om, ph, c, f);
+                    miss = slot - c >= f;    // c, slot < 2^24: c > slot wraps far above any f
                 }
-                rp += __popc(ball);
+                // misses are resolved by the whole warp, one lane at a time
+                uint32_t pending = __ballot_sync(0xFFFFFFFFu, miss);
+                while (pending) {
+                    const uint32_t Lm = __ffs(pending) - 1u;
+                    pending &= pending - 1u;
+                    cooperative_search<DT, EP>(a, Lm, slot, mu, rs, o, c, c + f, o, c, f);
+                }
+                if (active) {
+                    x = (uint64_t)f * (x >> m) + slot - c;
+                    // the decoded code replaces its (already read) mu code
+                    if (BITS == 16) reinterpret_cast<uint16_t *>(sw)[pi] = (uint16_t)K::code(o);
+                    else reinterpret_cast<uint8_t *>(sw)[pi] = (uint8_t)K::code(o);
+                }
+                // refill in lane order (FORMAT.md section 7); a read past the group's
+                // words returns stale ring data and is caught by the final checks
+                const bool refill = active && x < L;
+                const uint32_t ball = __ballot_sync(0xFFFFFFFFu, refill);
+                const uint32_t wd = ring[(rp + __popc(ball & lt)) & (kRing - 1)];
+                if (refill) x = (x << 32) | wd;
+                const uint32_t rp2 = rp + __popc(ball);
+                if ((rp2 ^ rp) >= kBlock) {
+                    __syncwarp();    // every lane's read of the block being replaced is done
+                    request((rp2 / kBlock) + 3u);
+                    cp_async_wait2();
+                    __syncwarp();
+                }
+                rp = rp2;
             }
         }
         if (active)
-            reinterpret_cast<uint4 *>(outp)[q] =
-                make_uint4(stage[0 * 32 + lane], stage[1 * 32 + lane], stage[2 * 32 + lane], stage[3 * 32 + lane]);
-    }
+            *ovp = make_uint4(stage[0 * 32 + lane], stage[1 * 32 + lane], stage[2 * 32 + lane], stage[3 * 32 + lane]);
+        mvp += g.W;
+        ovp += g.W;
+    };
+    // every lane has its vector j for j < nq_all (the group's last stream has the fewest)
+    const uint64_t nq_all = stream_vectors(g, cs.n_vec, grp * 32u + 31u);
+    uint64_t j = 0;
+    for (; j < nq_all; ++j) vector(std::false_type{}, j);
+    for (; j < nq0; ++j) vector(std::true_type{}, j);
     cp_async_wait0();
     corrupt |= (x != L);
-    if (lane == 0 && rp != nw) corrupt = true;
+    if (lane == 0 && rp != nw) corrupt = true;     // short of, or past, the group's words
     if (__any_sync(0xFFFFFFFFu, corrupt) && lane == 0) set_status(a.status, SKV_ERR_CORRUPT);
     if (__any_sync(0xFFFFFFFFu, bad_mu) && lane == 0) set_status(a.status, SKV_ERR_NONFINITE_MU);
 }
