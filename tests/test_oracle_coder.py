@@ -205,3 +205,32 @@ def test_input_errors():
     with pytest.raises(O.OracleError) as e:
         O.encode(lay, w["kv"], w["mu"], w["sigma"], np.zeros(65536, np.uint64))
     assert e.value.name == "EMPTY_MARGINAL"
+
+
+# The rate bound on every workload recipe (scaled to a few million scalars so
+# the oracle finishes in seconds): coded bits per scalar at most 1% above the
+# ideal cross-entropy of the real-valued mixture (blog information-theory
+# section: code length = -log2 q), and within the chunk header and flush
+# overhead of the integer model's own code length, so that a growth of either
+# fails here.
+@pytest.mark.parametrize("name,layers,tokens", [("tiny", None, None), ("qwen3_0p6b", 2, 1024),
+                                                ("qwen3_8b", 2, 2048), ("fp8_32b", 2, 2048),
+                                                ("paged_14b", 1, 2048)])
+def test_rate_bound_every_recipe(name, layers, tokens):
+    cfg = synth.CONFIGS[name]
+    if layers:
+        cfg = cfg.scaled(n_layers=layers, n_tokens=tokens)
+    w = synth.to_numpy(synth.generate(cfg))
+    dt = O.BF16 if cfg.dtype == "bf16" else O.E4M3
+    lay = _layout(dt, cfg.n_layers, cfg.n_kv, cfg.n_tokens, cfg.n_heads, cfg.head_dim)
+    s, offs = O.encode(lay, w["kv"], w["mu"], w["sigma"], w["counts"])
+    n = lay.n_elems
+    bits = _payload_bits(lay, s, offs) / n
+    ideal = O.ideal_bits(lay, w["kv"], w["mu"], w["sigma"], w["counts"]) / n
+    model = O.model_bits(lay, w["kv"], w["mu"], w["sigma"], w["counts"]) / n
+    assert bits <= 1.01 * ideal, (name, bits, ideal)
+    # per chunk: W final states (8 B), the group word counts padded to 16 B, and
+    # at most 12 B of padding per group's word array
+    W, G = lay.streams_per_chunk, lay.streams_per_chunk // 32
+    header = O.num_chunks(lay) * (8 * W + 16 * ((4 * G + 15) // 16) + 12 * G) * 8 / n
+    assert model <= bits <= model + header + 0.002, (name, model, bits, header)
