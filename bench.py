@@ -11,9 +11,11 @@ are far larger than the 129 MB L2, so no flush is needed between steps.
 
 --impl reference times the CPU oracle (oracle/), the only reference there is
 for this method, on a bounded sample of the same workload.
-Under torchrun (N > 1) every rank codes its own full workload (weak scaling):
-chunks are independent, there is no data-path collective; only the barrier
-and the max-over-ranks timing use NCCL.
+Under torchrun (N > 1) the one cache is sharded by layer (strong scaling):
+each rank codes its contiguous layers; the only exchanges are the all-reduce
+of the code histogram (p_hat is global side information) before coding and
+the all-gather of the ranks' byte totals that stitches their streams; rank 0
+checks the stitched total against a one-GPU encoding of the whole cache.
 """
 from __future__ import annotations
 
@@ -33,8 +35,8 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 # The format's own arithmetic per scalar, by instruction class: the totals
-# table of the SKV v1 format's section 9 (FORMAT.md), read from that file and
-# checked against the library's copy (skv_op_table). The arithmetic roofline
+# table of the SKV v1 format's section 9, read from the format text at the
+# repository root and checked against the library's copy (skv_op_table). The arithmetic roofline
 # is the scalars per second of the matching skv_peak_probe table probe.
 OP_CLASSES = ["fp32", "fminmax", "iadd", "logic", "shift", "iminmax", "imad", "imad_hi", "imad_wide",
               "cvt", "mufu", "popc", "vote", "lds", "ldt", "sts"]
@@ -42,7 +44,7 @@ OP_TABLES = [("bf16", "encode"), ("bf16", "decode"), ("e4m3", "encode"), ("e4m3"
 
 
 def op_tables(check_lib: bool = True) -> dict:
-    """{(dtype, op): {"counts": {class: n}, "instructions": n, "ops": weighted}} from FORMAT.md section 9."""
+    """{(dtype, op): {"counts": {class: n}, "instructions": n, "ops": weighted}} from SKV v1 format §9."""
     import re
     out = {}
     with open(os.path.join(ROOT, "FORMAT.md")) as fh:
@@ -52,11 +54,11 @@ def op_tables(check_lib: bool = True) -> dict:
                 continue
             v = [int(x) for x in m.group(3).split("|")]
             if len(v) != len(OP_CLASSES) + 2:
-                raise SystemExit(f"FORMAT.md section 9: malformed row {line.strip()}")
+                raise SystemExit(f"SKV v1 format §9: malformed row {line.strip()}")
             out[(m.group(1), m.group(2))] = {"counts": dict(zip(OP_CLASSES, v[:-2])), "instructions": v[-2],
                                              "ops": v[-1]}
     if sorted(out) != sorted(OP_TABLES):
-        raise SystemExit("FORMAT.md section 9: operation table rows missing")
+        raise SystemExit("SKV v1 format §9: operation table rows missing")
     if check_lib:
         import ctypes as C
         from lossless_kv_cache_scalar_gb300 import _binding as B
@@ -65,9 +67,9 @@ def op_tables(check_lib: bool = True) -> dict:
             counts, weights = (C.c_uint32 * n)(), (C.c_uint32 * n)()
             B.check("skv_op_table", B.lib().skv_op_table(t, counts, weights, n))
             if list(counts) != [out[key]["counts"][c] for c in OP_CLASSES]:
-                raise SystemExit(f"skv_op_table({key}) differs from FORMAT.md section 9")
+                raise SystemExit(f"skv_op_table({key}) differs from SKV v1 format §9")
             if sum(a * b for a, b in zip(counts, weights)) != out[key]["ops"]:
-                raise SystemExit(f"skv_op_table({key}) weights differ from FORMAT.md section 9")
+                raise SystemExit(f"skv_op_table({key}) weights differ from SKV v1 format §9")
     return out
 
 
@@ -158,6 +160,27 @@ def cpu_oracle_run(cfg, sample_chunks: int, nthreads: int, seconds_hint: float =
     return nbytes, dt, desc
 
 
+def cpu_table(single_chunks: int = 8, parallel_chunks: int = 64):
+    """The CPU oracle on every workload recipe: encode + decode throughput
+    (GB/s of uncompressed KV) single-threaded and chunk-parallel over all the
+    host's cores, each on a bounded sample of the recipe (1 layer, K and V,
+    the first tokens)."""
+    from lossless_kv_cache_scalar_gb300 import synth
+    from oracle import oracle as O
+    rows = {}
+    for name, cfg in synth.CONFIGS.items():
+        row = {}
+        for label, chunks, threads in (("single_thread", single_chunks, 1),
+                                       ("parallel", parallel_chunks, O.threads())):
+            nb, dt, desc = cpu_oracle_run(cfg, chunks, threads)
+            row[label] = {"gbs": nb / dt / 1e9, "threads": threads, "seconds": dt, "sample": desc}
+        rows[name] = row
+    import platform
+    print(json.dumps({"cpu_baseline_table": rows, "unit": "GB/s of uncompressed KV, encode + decode",
+                      "host": platform.machine(), "cores": O.threads()}), flush=True)
+    return 0
+
+
 def run_reference(args, cfg):
     world, rank, _ = _dist()
     if rank != 0:
@@ -221,10 +244,15 @@ def main():
     ap.add_argument("--model-inputs", type=int, default=1,
                     help="time skv_histogram and skv_calibrate_sigma on the workload (0: skip)")
     ap.add_argument("--traffic-json", default=os.path.join(ROOT, "profiles", "traffic.json"))
+    ap.add_argument("--cpu-table", action="store_true",
+                    help="only time the CPU oracle on every workload recipe (single-thread and chunk-parallel "
+                         "samples) and print that table as one JSON line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "skv" else args.warmup
 
     from lossless_kv_cache_scalar_gb300 import synth
+    if args.cpu_table:
+        return cpu_table()
     cfg = synth.CONFIGS[args.config]
     if args.layers or args.tokens:
         cfg = cfg.scaled(n_layers=args.layers, n_tokens=args.tokens)
@@ -238,8 +266,22 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    cfg = cfg.scaled(seed=cfg.seed + 1000 * rank) if world > 1 else cfg
-    w = synth.generate(cfg, device=dev, with_mask=args.sigma_block > 0)
+    # One cache, sharded by layer (the path's own partition): every rank draws
+    # the same cache, keeps its contiguous layers, counts their codes on the
+    # GPU and all-reduces the histogram (p_hat is global); N = 1 is the whole
+    # cache on one GPU.
+    from lossless_kv_cache_scalar_gb300 import shard
+    w_all = synth.generate(cfg, device=dev, with_mask=args.sigma_block > 0)
+    rng, part, counts = shard.rank_inputs(w_all, rank, world, lambda kv: skv.histogram(kv, cfg.dtype))
+    if world == 1 and not torch.equal(counts, w_all["counts"]):
+        raise SystemExit("bench: skv_histogram differs from the workload's counts")
+    w = dict(part, counts=counts)
+    if "mask" in w_all:
+        w["mask"] = w_all["mask"][rng.first: rng.first + rng.count]
+    full_layers = cfg.n_layers
+    cfg = cfg.scaled(n_layers=rng.count)
+    del w_all
+    torch.cuda.empty_cache()
     lay = skv.Layout(cfg.dtype, cfg.n_layers, cfg.n_kv, cfg.n_heads, cfg.head_dim, cfg.n_tokens,
                      streams_per_chunk=args.streams, sigma_block_tokens=args.sigma_block)
     if args.sigma_block:
@@ -295,12 +337,20 @@ def main():
         t = torch.tensor([t_tot, t_enc, t_dec], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         t_tot, t_enc, t_dec = t.tolist()
-    value = world * raw_bytes * args.steps / t_tot / 1e9
+    # the whole cache's bytes (every rank's layers) over the slowest rank's time
+    cache_bytes = raw_bytes * full_layers // max(cfg.n_layers, 1) if world > 1 else raw_bytes
+    if world > 1:
+        t = torch.tensor([raw_bytes], device=dev, dtype=torch.int64)
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        cache_bytes = int(t.item())
+    value = cache_bytes * args.steps / t_tot / 1e9
+    # this rank's byte base in the stitched stream and the cache's total
+    base, stitched_total = shard.distributed_base(total_bytes, device=dev) if world > 1 else (0, total_bytes)
     enc_gbs = raw_bytes * args.steps / t_enc / 1e9
     dec_gbs = raw_bytes * args.steps / t_dec / 1e9
 
     # roofline of the dominant kernel (encode or decode call): the format's
-    # operations per scalar (FORMAT.md section 9) over the rate at which the
+    # operations per scalar (SKV v1 format §9) over the rate at which the
     # table probe runs that same operation mix on this GPU
     dom = "decode" if t_dec >= t_enc else "encode"
     t_dom = (t_dec if dom == "decode" else t_enc) / args.steps
@@ -316,7 +366,7 @@ def main():
     except (OSError, ValueError):
         traffic = None
     hbm_peak = _peaks().get("hbm_gbs", 6685.5)
-    probes = alu_peaks(dev) if args.alu_probe else None
+    probes = alu_peaks(dev) if (args.alu_probe and rank == 0) else None
 
     def arith(op, t_total):
         """(achieved Tops, peak Tops, frac, frac against the uniform issue peak) for one direction."""
@@ -328,16 +378,43 @@ def main():
 
     a_enc, a_dec = arith("encode", t_enc), arith("decode", t_dec)
     achieved, peak_tops, frac, frac_uniform = a_dec if dom == "decode" else a_enc
-    page_lat = page_latency(coder, out, offsets, w, lay, args, dev) if args.page_latency else None
-    inputs = model_inputs_run(w, lay, args, dev, hbm_peak) if args.model_inputs else None
-    offload = offload_run(coder, out, offsets, w, lay, args, dev, total_bytes) if args.offload else None
-    requant = requant_run(w, lay, dev, hbm_peak) if (args.requant and lay.dtype == "bf16") else None
-    bits = 8.0 * total_bytes / n_el
+    # per-GPU characterisations: rank 0 on its own layers
+    lead = rank == 0
+    page_lat = page_latency(coder, out, offsets, w, lay, args, dev) if (args.page_latency and lead) else None
+    inputs = model_inputs_run(w, lay, args, dev, hbm_peak) if (args.model_inputs and lead) else None
+    offload = offload_run(coder, out, offsets, w, lay, args, dev, total_bytes) if (args.offload and lead) else None
+    requant = requant_run(w, lay, dev, hbm_peak) if (args.requant and lay.dtype == "bf16" and lead) else None
+    bits = 8.0 * stitched_total / (cache_bytes / lay.bytes_per_code)
 
-    # end to end through the public API with host buffers
+    # end to end through the public API with host buffers, every rank on its layers
     e2e = None
     if not args.no_e2e:
+        barrier()
         e2e = e2e_run(coder, w, lay, args, dev, total_bytes)
+        if world > 1:
+            tmax = torch.tensor([e2e["seconds"]], device=dev, dtype=torch.float64)
+            dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+            sums = torch.tensor([lay.n_elems * lay.bytes_per_code, e2e["h2d_bytes_per_step"],
+                                 e2e["d2h_bytes_per_step"]], device=dev, dtype=torch.int64)
+            dist.all_reduce(sums, op=dist.ReduceOp.SUM)
+            e2e["value"] = int(sums[0]) * e2e["steps"] / float(tmax[0]) / 1e9
+            e2e["h2d_bytes_per_step"], e2e["d2h_bytes_per_step"] = int(sums[1]), int(sums[2])
+            e2e["seconds"] = float(tmax[0])
+    # N > 1: the stitched total equals the one-GPU encoding of the whole cache
+    single_total = None
+    if world > 1 and lead:
+        wf = synth.generate(synth.CONFIGS[args.config].scaled(n_layers=args.layers, n_tokens=args.tokens)
+                            if (args.layers or args.tokens) else synth.CONFIGS[args.config], device=dev)
+        del coder, out, back
+        torch.cuda.empty_cache()
+        layf = skv.Layout(cfg.dtype, full_layers, cfg.n_kv, cfg.n_heads, cfg.head_dim, cfg.n_tokens,
+                          streams_per_chunk=args.streams)
+        cf = skv.Coder(layf, dev)
+        sf, of = cf.encode(wf["kv"], wf["mu"], wf["sigma"], wf["counts"])
+        single_total = int(of[-1].item())
+        del wf, cf, sf, of
+        if single_total != stitched_total:
+            raise SystemExit(f"bench: stitched total {stitched_total} != one-GPU total {single_total}")
     line = None
     if rank == 0:
         cpu = None
@@ -354,10 +431,14 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * t_tot / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "u32/u64 int + f32", "data": "synthetic",
-            "config": {"workload": cfg.name, "shape": [cfg.n_layers, cfg.n_kv, cfg.n_tokens, cfg.n_heads,
+            "scaling": "strong", "vs_baseline": None, "dtype": "u32/u64 int + f32", "data": "synthetic",
+            "config": {"workload": cfg.name, "shape": [full_layers, cfg.n_kv, cfg.n_tokens, cfg.n_heads,
                                                        cfg.head_dim],
-                       "code_dtype": cfg.dtype, "scalars": n_el, "tokens_per_chunk": lay.tokens_per_chunk,
+                       "sharding": (f"layers split over {world} GPUs ({rng.count} on rank 0), p_hat counts "
+                                    "all-reduced, byte bases all-gathered" if world > 1 else "one GPU, all layers"),
+                       "stitched_bytes": stitched_total, "one_gpu_bytes": single_total if world > 1 else stitched_total,
+                       "code_dtype": cfg.dtype, "scalars": cache_bytes // lay.bytes_per_code,
+                       "tokens_per_chunk": lay.tokens_per_chunk,
                        "streams_per_chunk": lay.streams_per_chunk, "weights": list(lay.weights),
                        "sigma_block_tokens": lay.sigma_block_tokens,
                        "l2": "inputs 2 x %.1f GB >> 129 MB L2, no flush" % (raw_bytes / 1e9)},
@@ -370,7 +451,7 @@ def main():
                          "alg_instructions_per_scalar": tables[(lay.dtype, dom)]["instructions"],
                          "ncu_thread_inst_per_scalar": inst_per_scalar,
                          "peak_basis": ("measured: skv_peak_probe running the format's %s %s operation table "
-                                        "(FORMAT.md section 9) with full instruction-level parallelism"
+                                        "(SKV v1 format §9) with full instruction-level parallelism"
                                         % (lay.dtype, dom)) if probes else "not measured (--alu-probe 0)",
                          "frac_of_uniform_issue": frac_uniform,
                          "uniform_issue_tops": uniform_tops,
@@ -581,8 +662,8 @@ def requant_run(w, lay, dev, hbm_peak, reps=5, group=128):
 
 
 def alu_peaks(dev, target_ms=20.0):
-    """skv_peak_probe: the rate of each instruction class of FORMAT.md
-    section 9 alone (Tops/s, 32-bit operations) and of each whole operation
+    """skv_peak_probe: the rate of each instruction class of the SKV v1
+    format's section 9 alone (Tops/s, 32-bit operations) and of each whole operation
     table (scalars/s), each the best of 3 launches sized to about target_ms."""
     import ctypes as C
     from lossless_kv_cache_scalar_gb300 import _binding as B
@@ -668,7 +749,7 @@ def e2e_run(coder, w, lay, args, dev, total_bytes):
     raw = lay.n_elems * lay.bytes_per_code
     h2d = 2 * raw + total_bytes + raw + 2 * 8 * (lay.n_chunks + 1) + sig_h.numel() * 4 + cnt_h.numel() * 8
     d2h = total_bytes + 8 * (lay.n_chunks + 1) + raw
-    return {"value": raw * steps / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+    return {"value": raw * steps / dt / 1e9, "unit": "GB/s", "seconds": dt, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "layers_per_batch": hc.lpb,
             "encode_host_ms": 1e3 * float(np.median(t_enc)), "decode_host_ms": 1e3 * float(np.median(t_dec)),
             "timing": "host wall clock around skv_encode_host (host KV, mu -> host bitstream) and "

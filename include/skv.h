@@ -11,8 +11,8 @@
  * length approaches -log2 q(x) (information-theory section of the blog
  * "推测性KV编码：用预测模型实现缓存无损压缩4倍", blog.hotdry.top), and the
  * CDF must be bit-identical at both ends (that blog's deployment section).
- * The integer discretisation and the bitstream are specified in FORMAT.md
- * (version 1).
+ * The integer discretisation and the bitstream are specified by the SKV
+ * bitstream format, version 1 (its sections are cited as "SKV v1 format §N").
  *
  * Conventions for every entry point:
  *  - Pointers named as device pointers must point to device memory of the
@@ -47,7 +47,7 @@ extern "C" {
 
 #define SKV_FORMAT_VERSION 1u
 
-/* Code types (FORMAT.md section 1). */
+/* Code types (SKV v1 format §1). */
 enum { SKV_BF16 = 0, SKV_E4M3 = 1 };
 
 /* Status codes: returned by calls (host-detected) or written to *status (device-detected). */
@@ -64,7 +64,7 @@ enum {
 };
 
 /*
- * What is coded and how it is cut (FORMAT.md sections 4 and 7).
+ * What is coded and how it is cut (SKV v1 format §4 and §7).
  *  version            SKV_FORMAT_VERSION
  *  dtype              SKV_BF16 or SKV_E4M3
  *  n_layers, n_kv     planes; n_kv is 2 for K and V
@@ -123,7 +123,7 @@ int32_t skv_layout_check(const skv_layout *lay);
 int32_t skv_num_chunks(const skv_layout *lay, uint64_t *n_chunks);
 
 /*
- * Upper bound on the encoded size in bytes (FORMAT.md section 8): an
+ * Upper bound on the encoded size in bytes (SKV v1 format §8): an
  * out_capacity of this size never gives SKV_ERR_CAPACITY. About 1.56x the
  * raw bf16 bytes and 2.1x the raw e4m3 bytes, reached only by data the model
  * predicts very badly.
@@ -263,6 +263,12 @@ int32_t skv_decode_offload(const skv_layout *lay, const void *host_bitstream, ui
  *                  finished this call's work
  * Offsets that descend, pass bitstream_bytes or are not 16-byte multiples
  * return SKV_ERR_CORRUPT. Device errors as skv_decode_chunks_prepared.
+ * Host buffers: host_offsets is read only during the call. host_chunk_ids and
+ * the listed pages of host_bitstream are also the sources of asynchronous
+ * copies on copy_stream: from pageable memory CUDA stages them before the call
+ * returns, but from pinned memory they are read when copy_stream runs, so a
+ * pinned host_chunk_ids or host_bitstream must stay unchanged until
+ * copy_stream has passed this call's copies (e.g. until stream has finished).
  */
 int32_t skv_decode_pages_host(const skv_layout *lay, const void *host_bitstream, uint64_t bitstream_bytes,
                               const uint64_t *host_offsets, const void *mu, const uint32_t *host_chunk_ids,
@@ -286,7 +292,7 @@ int32_t skv_offload_plan(const uint64_t *host_offsets, uint64_t n_chunks, uint64
                          uint64_t *n_batches);
 
 /*
- * Evaluate the model's cumulative frequency C(o) (FORMAT.md section 5) for n
+ * Evaluate the model's cumulative frequency C(o) (SKV v1 format §5) for n
  * independent queries: C[i] = C(ords[i]) for predictor code mu_codes[i] and
  * scale sigmas[i], under the weights of lay and the marginal counts. For
  * checking the model kernel against an independent implementation.
@@ -456,14 +462,21 @@ int32_t skv_search_eval(const skv_layout *lay, const uint64_t *counts, uint64_t 
  * Its scratch is a fixed device array of SKV_NOALLOC_SCRATCH_BYTES inside the
  * library, held by every GPU that loads the library until the process exits.
  * Layouts whose minimum decode scratch (skv_workspace_bytes(lay, 0, ...): the
- * P_hat and quantile tables plus 4 bytes per (layer, kv, channel)) exceeds it
- * are rejected with SKV_ERR_INVALID_ARG before anything is enqueued; 1 MiB
- * covers a bf16 cache of up to 193,920 (layer, kv, channel) sigmas, e.g. 80
- * planes (40 layers, K and V) of 2,048 channels. The outlier inverse tables do
- * not fit, so far outliers are found by bisection (same output, slower).
+ * P_hat and quantile tables plus 4 bytes per sigma entry, i.e. per (layer, kv,
+ * sigma block, channel)) exceeds it are rejected with SKV_ERR_INVALID_ARG
+ * before anything is enqueued; for bf16, 1 MiB covers up to 193,920 sigma
+ * entries, e.g. 80 planes (40 layers, K and V) of 2,048 channels with one
+ * sigma per channel, or fewer planes when the layout has several sigma blocks.
+ * The bf16 decoder's optional tables (the (edge, P_hat) pairs and the outlier
+ * inverse tables, tens of MiB) do not fit, so its far outliers are found by
+ * bisection (same output, slower); an e4m3 layout's full workspace is small
+ * and, when it fits, the call uses it whole.
  *
  * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture. Every call
+ * device current); make that first call before any stream capture. The
+ * address is kept for the life of the process: after a cudaDeviceReset the
+ * library's device array (and that address) no longer exist, so do not call
+ * this entry point again in the same process after a reset. Every call
  * on a device shares the one array and each call rewrites all of it that it
  * reads, so nothing carries over between calls; calls that overlap on the GPU
  * (on different streams, or from several host threads) race on it and must be

@@ -3,7 +3,7 @@
 Every translation unit is compiled for sm_103a only
 (-gencode arch=compute_103a,code=sm_103a), in parallel, then linked into one
 shared library next to this file. No fast-math and no flush-to-zero: the
-model's binary32 steps must round exactly as FORMAT.md section 5 writes them.
+model's binary32 steps must round exactly as SKV v1 format §5 writes them.
 """
 from __future__ import annotations
 

@@ -32,7 +32,7 @@ int launch_search_aids(const Geom &g, const uint32_t *phat, float *qt, uint16_t 
 
 // ------------------------------------------------------------- set-up kernel
 
-// P_hat(o) = floor(2^24 cum(o) / total) exactly (FORMAT.md section 5): a
+// P_hat(o) = floor(2^24 cum(o) / total) exactly (SKV v1 format §5): a
 // binary32 estimate cum * (2^24 / total), within a few units of the result,
 // then integer correction with 128-bit products. `scale` = 2^24 / total is
 // computed once per thread (binary64 division is slow, and the set-up builds
@@ -248,7 +248,7 @@ static int32_t make_geom(const skv_layout *lay, Geom &g) {
     return SKV_OK;
 }
 
-// Worst-case bytes of one chunk with n_vec vectors (FORMAT.md section 8).
+// Worst-case bytes of one chunk with n_vec vectors (SKV v1 format §8).
 static uint64_t chunk_max_bytes(const Geom &g, uint64_t n_vec) {
     const DtypeInfo d = dtype_info(g.dtype);
     uint64_t b = g.hdr_bytes;

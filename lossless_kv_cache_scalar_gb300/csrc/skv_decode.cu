@@ -1,5 +1,5 @@
 // skv_decode.cu -- decoder: CDF inversion fused with the rANS state update and
-// word refill (FORMAT.md sections 5-7), plus the per-call search aids.
+// word refill (SKV v1 format §§5-7), plus the per-call search aids.
 //
 // The decoder of the Speculative KV Coding wiki's pipeline section: from the
 // bits and the same (mu, sigma) it restores every code exactly. One warp
@@ -16,7 +16,7 @@
 // code, the slot gives a quantile g of G(z) = (w_n Phi(z) + w_w Phi(z/3)) /
 // (w_n + w_w); a table in t = -log2(min(g, 1 - g)) gives z = G^-1(g); and
 // mu + z sigma rounded to the code grid is the estimate (a code owns the reals
-// that round to it, FORMAT.md section 2). A first pass takes the reference at
+// that round to it, SKV v1 format §2). A first pass takes the reference at
 // mu's own code, a second (bf16) at the first estimate. A far outlier that only
 // p_hat explains (both Gaussians saturated, so C is a mu-independent function
 // of o) is read from per-call inverse tables instead. When the test fails,
@@ -457,7 +457,7 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
         stage[3 * 32 + lane] = muv.w;
         {
             // a non-finite mu code anywhere in the vector (rare): report it and
-            // model those elements with mu = +0 (FORMAT.md section 4). A part of
+            // model those elements with mu = +0 (SKV v1 format §4). A part of
             // t is zero exactly where a code's exponent field is all ones.
             constexpr uint32_t E = BITS == 16 ? 0x7F807F80u : 0x7F7F7F7Fu;
             constexpr uint32_t ONE = BITS == 16 ? 0x00010001u : 0x01010101u;
@@ -516,7 +516,7 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
                     if (BITS == 16) reinterpret_cast<uint16_t *>(sw)[pi] = (uint16_t)K::code(o);
                     else reinterpret_cast<uint8_t *>(sw)[pi] = (uint8_t)K::code(o);
                 }
-                // refill in lane order (FORMAT.md section 7); a read past the group's
+                // refill in lane order (SKV v1 format §7); a read past the group's
                 // words returns stale ring data and is caught by the final checks
                 const bool refill = active && x < L;
                 const uint32_t ball = __ballot_sync(0xFFFFFFFFu, refill);

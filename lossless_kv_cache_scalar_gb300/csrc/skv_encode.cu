@@ -1,5 +1,5 @@
 // skv_encode.cu -- encoder kernels: per-scalar model + warp-interleaved rANS,
-// chunk-size scan, and compaction into the final bitstream (FORMAT.md 6-7).
+// chunk-size scan, and compaction into the final bitstream (SKV v1 format §6-7).
 //
 // The encoder is the "arithmetic coder emits bits" box of the Speculative KV
 // Coding wiki's pipeline section, in its rANS form. One warp owns one group of
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(EncShape<DT>::warps * 32, 1) encode_kernel(con
     }
 }
 
-// Per-chunk sizes (FORMAT.md section 7) and their exclusive scan into offsets.
+// Per-chunk sizes (SKV v1 format §7) and their exclusive scan into offsets.
 __global__ void __launch_bounds__(1024) scan_kernel(const ScanArgs a) {
     const Geom &g = a.g;
     __shared__ uint64_t warp_tot[32];

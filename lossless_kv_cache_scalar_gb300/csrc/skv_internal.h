@@ -1,6 +1,6 @@
 // skv_internal.h -- host/device shared geometry and kernel argument blocks.
 //
-// Geometry follows FORMAT.md section 7: a chunk is one (layer, kv, page of
+// Geometry follows SKV v1 format §7: a chunk is one (layer, kv, page of
 // tokens_per_chunk tokens) block, contiguous in the canonical layout; it has
 // G = W/32 groups of 32 interleaved rANS streams; stream s = 32 g + lane owns
 // the 16-byte vectors q with q mod W == s.
@@ -140,7 +140,7 @@ struct InvArgs {
     uint16_t *inv_hi;      // M entries: max{o : C_hi(o) <= s} (0 if none)
 };
 
-// decode_kernel keeps 4 CTAs of 8 warps resident per SM (its launch bounds).
+// decode_kernel keeps one persistent CTA of 32 warps resident per SM (its launch bounds).
 constexpr uint32_t kDecResidentWarps = 32;
 
 struct DecArgs {

@@ -3,7 +3,7 @@
 // The model is the three-component mixture of the Speculative KV Coding wiki
 // (mixture section): 0.95 N(mu, sigma^2) + 0.03 N(mu, (3 sigma)^2) +
 // 0.02 p_hat, integrated over each code's rounding interval. Its integer form
-// (FORMAT.md section 5) must be bit-identical at encoder and decoder, which
+// (SKV v1 format §5) must be bit-identical at encoder and decoder, which
 // the 推测性KV编码 blog's deployment section demands of any arithmetic coder:
 // every float step below is one IEEE binary32 operation with round-to-nearest,
 // written with explicit _rn intrinsics so nothing is contracted into an FMA,
@@ -17,7 +17,7 @@
 
 namespace skv {
 
-// T[j + 2048] = round_half_even(2^24 Phi(j / 256)), FORMAT.md section 3.
+// T[j + 2048] = round_half_even(2^24 Phi(j / 256)), SKV v1 format §3.
 static __device__ const uint32_t kPhiQ24[4097] = {SKV_PHI_Q24_VALUES};
 
 // Tables staged in shared memory by every CTA that evaluates the model: the
@@ -57,7 +57,7 @@ template <> struct Codes<SKV_BF16> {
     }
     __device__ __forceinline__ static bool finite(uint32_t b) { return (b & 0x7F80u) != 0x7F80u; }
     __device__ __forceinline__ static float value(uint32_t b) { return __uint_as_float(b << 16); }
-    // Edge E(o) (FORMAT.md section 2) straight from the bits: for a positive code
+    // Edge E(o) (SKV v1 format §2) straight from the bits: for a positive code
     // k >= 1 the binary32 pattern (k << 16) - 0x8000 lies half a bf16 step below
     // code k, which is the exact midpoint of codes k-1 and k (binary32 spacing is
     // uniform within a binade and the bf16 grid is a subset of it); negative
@@ -118,7 +118,7 @@ template <> struct Codes<SKV_E4M3> {
     }
 };
 
-// Edge of ordinal o computed from the code values (FORMAT.md section 2), used to
+// Edge of ordinal o computed from the code values (SKV v1 format §2), used to
 // fill the e4m3 edge table; the bf16 path uses the equivalent bit form above.
 template <uint32_t DT>
 __device__ float edge_from_values(uint32_t o) {
@@ -155,7 +155,7 @@ __device__ void stage_tables(PhiTables<WIDE> &t, Tables8 &t8, const uint32_t *__
 
 // -------------------------------------------------------------- model: C(o)
 //
-// C(o) of FORMAT.md section 5 in a form that keeps most steps on the binary32
+// C(o) of SKV v1 format §5 in a form that keeps most steps on the binary32
 // pipe, each step exact:
 //  - zq = floor(z 2^16): one multiply-add rounded down, z 2^16 + 1.5 2^23,
 //    whose exact value lies in [2^23, 2^24) where binary32 spacing is 1, so the

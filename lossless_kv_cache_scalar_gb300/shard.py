@@ -1,6 +1,6 @@
 """Sharding a KV cache across ranks by layer, and stitching the bitstreams.
 
-Chunks are independent (FORMAT.md section 7), so the coder shards with no
+Chunks are independent (SKV v1 format §7), so the coder shards with no
 data-path exchange: each rank codes a contiguous range of layers as a layout
 of its own, and the one global bitstream is the ranks' streams back to back.
 The only exchange is an exclusive scan of the per-rank byte totals, which
@@ -59,12 +59,13 @@ def stitch(local_streams: list[torch.Tensor], local_offsets: list[torch.Tensor])
     return torch.cat([s.reshape(-1) for s in local_streams]), torch.cat(offs)
 
 
-def distributed_base(local_total: int, group=None) -> tuple[int, int]:
-    """(this rank's byte base, global total) via an all-gather of the totals."""
+def distributed_base(local_total: int, group=None, device=None) -> tuple[int, int]:
+    """(this rank's byte base, global total) via an all-gather of the totals
+    (device: where the collective's tensors live, e.g. the rank's GPU for NCCL)."""
     import torch.distributed as dist
     world = dist.get_world_size(group)
-    t = torch.tensor([int(local_total)], dtype=torch.int64)
-    got = [torch.zeros(1, dtype=torch.int64) for _ in range(world)]
+    t = torch.tensor([int(local_total)], dtype=torch.int64, device=device)
+    got = [torch.zeros(1, dtype=torch.int64, device=device) for _ in range(world)]
     dist.all_gather(got, t, group=group)
     totals = [int(x.item()) for x in got]
     return exclusive_bases(totals)[dist.get_rank(group)], sum(totals)
@@ -76,3 +77,22 @@ def allreduce_counts(local_counts: torch.Tensor, group=None) -> torch.Tensor:
     c = local_counts.to(torch.int64).clone()
     dist.all_reduce(c, op=dist.ReduceOp.SUM, group=group)
     return c
+
+
+def rank_inputs(cache: dict, rank: int, world: int, histogram, group=None):
+    """This rank's share of one cache and the global code histogram.
+
+    cache: {"kv", "mu", "sigma"} with the layer as the outermost dimension
+    (the canonical [L][n_kv][T][H][D] codes and [L][n_kv][H][D] sigma).
+    histogram(kv_part) -> int64 counts of the rank's own codes (on the device
+    the collective runs on). Returns (LayerRange, {"kv", "mu", "sigma"} views
+    of the rank's layers, global counts): the counts are all-reduced, since
+    p_hat is one global table both ends hold.
+    """
+    n_layers = cache["kv"].shape[0]
+    rng = layer_ranges(n_layers, world)[rank]
+    sl = slice(rng.first, rng.first + rng.count)
+    part = {k: cache[k][sl] for k in ("kv", "mu", "sigma")}
+    local = histogram(part["kv"])
+    counts = allreduce_counts(local, group) if world > 1 else local.to(torch.int64)
+    return rng, part, counts

@@ -1,8 +1,9 @@
 """Compile the CPU oracle into oracle/libskv_oracle.so.
 
-TEST INFRASTRUCTURE: the oracle is the checker of the CUDA library (see
-oracle/README.md). Plain gcc, C11, -O2, no FMA contraction, no fast-math, so
-the binary32 steps of FORMAT.md section 5 round exactly as written on x86-64
+TEST INFRASTRUCTURE: the oracle is the checker of the CUDA library, loaded
+only by the tests, the smoke check and the benchmark's CPU-baseline leg.
+Plain gcc, C11, -O2, no FMA contraction, no fast-math, so
+the binary32 steps of SKV v1 format §5 round exactly as written on x86-64
 and on aarch64 alike.
 """
 from __future__ import annotations

@@ -1,5 +1,5 @@
 /*
- * skv_oracle.c -- plain, slow CPU oracle of the SKV v1 format (FORMAT.md).
+ * skv_oracle.c -- plain, slow CPU oracle of the SKV v1 format.
  *
  * TEST INFRASTRUCTURE. This file is the checker, not the product: only the
  * tests, __graft_entry__.smoke() and bench.py's CPU-baseline leg (and its
@@ -15,12 +15,12 @@
  *   - "推测性KV编码：用预测模型实现缓存无损压缩4倍" (blog.hotdry.top): the
  *     information-theory section (code length = -log q, Gaussian cost) and the
  *     deployment section (bit-identical CDF on both ends).
- * The discretisation and the bitstream are FORMAT.md's; each function below
- * names the FORMAT.md section it writes out.
+ * The discretisation and the bitstream are the SKV v1 format's; each function below
+ * names the format section it writes out.
  *
  * Build: gcc -std=c11 -O2 -ffp-contract=off -fno-fast-math -fPIC -shared
  *        -pthread (oracle/build.py). No FMA contraction and no flush-to-zero:
- *        the fp32 steps of FORMAT.md section 5 must round exactly as written.
+ *        the fp32 steps of SKV v1 format §5 must round exactly as written.
  *
  * Parity pins for every function are in tests/test_oracle_*.py.
  */
@@ -44,7 +44,7 @@ enum {
 
 enum { DT_BF16 = 0, DT_E4M3 = 1 };
 
-/* FORMAT.md section 3: T[j + 2048] = round_half_even(2^24 Phi(j/256)). */
+/* SKV v1 format §3: T[j + 2048] = round_half_even(2^24 Phi(j/256)). */
 static const uint32_t PHI_T[4097] = {
 #include "phi_q24.inc"
 };
@@ -60,7 +60,7 @@ typedef struct {
     uint32_t sigma_block;  /* 0: one sigma per channel; else tokens per sigma block */
 } or_layout;
 
-typedef struct {          /* per-dtype constants, FORMAT.md section 1 */
+typedef struct {          /* per-dtype constants, SKV v1 format §1 */
     uint32_t N;           /* number of codes */
     uint32_t m;           /* M = 2^m */
     uint32_t V;           /* scalars per 16-byte vector */
@@ -208,7 +208,7 @@ static int sigma_valid(float s)
 }
 
 /* The model value of a mu code: non-finite mu is reported and replaced by 0
-   (FORMAT.md section 4). */
+   (SKV v1 format §4). */
 static float mu_value(uint32_t dtype, uint32_t code, int *bad)
 {
     if (!code_is_finite(dtype, code)) { *bad = 1; return 0.0f; }
@@ -329,7 +329,7 @@ static int geom_init(const or_layout *lay, or_geom *g)
     return OR_OK;
 }
 
-/* FORMAT.md section 4: the sigma entry of global element i. Without sigma
+/* SKV v1 format §4: the sigma entry of global element i. Without sigma
    blocks it is the element's (layer, kv, channel); with blocks of B tokens
    also its token's block t / B. */
 static uint64_t sigma_index(const or_geom *g, uint64_t i)
@@ -376,7 +376,7 @@ static uint64_t header_bytes(const or_geom *g)
     return 8ull * g->W + pad16(4ull * g->G);
 }
 
-/* Worst-case group words, FORMAT.md section 8. */
+/* Worst-case group words, SKV v1 format §8. */
 static uint64_t group_cap_words(const or_geom *g, uint64_t n_vec, uint32_t grp)
 {
     uint64_t nmax = stream_len(g, n_vec, 32 * grp);

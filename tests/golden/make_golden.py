@@ -1,5 +1,5 @@
 """Write tests/golden/oracle_tiny.json: a digest of the oracle's bitstream for
-the `tiny` synthetic workload (FORMAT.md v1). Calls only the oracle and the
+the `tiny` synthetic workload (the SKV v1 format). Calls only the oracle and the
 seeded input generator; run it again only when the format itself changes,
 and say in the commit which reading of the pages justified the change.
 """

@@ -1,5 +1,5 @@
 """The C-ABI library builds, loads and exports every symbol include/skv.h declares;
-its host-side geometry agrees with FORMAT.md (checked against the oracle's
+its host-side geometry agrees with the SKV v1 format (checked against the oracle's
 sizes). No GPU work is done here.
 """
 import ctypes as C

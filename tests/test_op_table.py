@@ -1,4 +1,4 @@
-"""The operation count of the format (FORMAT.md section 9) that defines the
+"""The operation count of the format (SKV v1 format §9) that defines the
 arithmetic roofline: the totals table, the per-step tables it sums, the
 library's copy (skv_op_table) and bench.py's reader agree. No GPU work.
 """

@@ -1,4 +1,4 @@
-"""Pins of the oracle's coder (FORMAT.md sections 6-7) against what the pages fix.
+"""Pins of the oracle's coder (SKV v1 format §§6-7) against what the pages fix.
 
 - Lossless: decode(encode(x)) == x bit for bit (wiki pipeline section: the
   decoder restores KV_full from the bits and (mu, sigma) alone).

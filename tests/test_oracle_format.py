@@ -1,4 +1,4 @@
-"""Pins of the oracle's alphabet, edges and fixed-point Phi (FORMAT.md sections 1-3).
+"""Pins of the oracle's alphabet, edges and fixed-point Phi (SKV v1 format §§1-3).
 
 Each check compares the oracle with something other than itself: exact
 rational arithmetic on the code values, numpy's own bf16/e4m3 decoding via

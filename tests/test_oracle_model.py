@@ -1,4 +1,4 @@
-"""Pins of the oracle's cumulative frequencies C(o) and its inversion (FORMAT.md section 5).
+"""Pins of the oracle's cumulative frequencies C(o) and its inversion (SKV v1 format §5).
 
 The integer model is compared with the real-valued mixture of the Speculative
 KV Coding wiki (mixture section), evaluated in double precision with libm's

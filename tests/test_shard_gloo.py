@@ -39,11 +39,12 @@ def _worker(rank, world, port, out_dir):
     os.environ["MASTER_PORT"] = str(port)
     dist.init_process_group("gloo", rank=rank, world_size=world)
     w = synth.to_numpy(synth.generate(CFG))
-    rng = shard.layer_ranges(CFG.n_layers, world)[rank]
-    sl = slice(rng.first, rng.first + rng.count)
-    kv, mu, sig = w["kv"][sl], w["mu"][sl], w["sigma"][sl]
-    local = torch.from_numpy(np.bincount(kv.reshape(-1), minlength=65536).astype(np.int64))
-    counts = shard.allreduce_counts(local).numpy().astype(np.uint64)
+    cache = {k: torch.from_numpy(w[k]) for k in ("kv", "mu", "sigma")}
+    # the bench's sharding path, with the oracle's histogram as the rank's counter
+    hist = lambda kv: torch.from_numpy(O.histogram(O.BF16, kv.numpy()).astype(np.int64))
+    rng, part, counts = shard.rank_inputs(cache, rank, world, hist)
+    kv, mu, sig = part["kv"].numpy(), part["mu"].numpy(), part["sigma"].numpy()
+    counts = counts.numpy().astype(np.uint64)
     assert np.array_equal(counts, w["counts"])
     lay = O.Layout(O.BF16, rng.count, CFG.n_kv, CFG.n_heads, CFG.head_dim, CFG.n_tokens)
     s, offs = O.encode(lay, kv, mu, sig, counts, nthreads=2)

@@ -31,11 +31,17 @@ def _noalloc(lay, bits, offs, mu, sigma, counts, out, status):
                                       C.c_void_p(s.cuda_stream))
 
 
-@pytest.mark.parametrize("name,kw", [("tiny", {}), ("fp8_32b", dict(n_layers=2, n_tokens=600))])
-def test_noalloc_decode_matches_decode_twice(name, kw):
+@pytest.mark.parametrize("name,kw,sblk", [("tiny", {}, 0), ("fp8_32b", dict(n_layers=2, n_tokens=600), 0),
+                                          ("qwen3_0p6b", dict(n_layers=3, n_tokens=1024), 256)])
+def test_noalloc_decode_matches_decode_twice(name, kw, sblk):
     cfg = synth.CONFIGS[name].scaled(**kw) if kw else synth.CONFIGS[name]
     w = {k: v.cuda() for k, v in synth.generate(cfg).items()}
-    lay = Layout(cfg.dtype, cfg.n_layers, cfg.n_kv, cfg.n_heads, cfg.head_dim, cfg.n_tokens)
+    lay = Layout(cfg.dtype, cfg.n_layers, cfg.n_kv, cfg.n_heads, cfg.head_dim, cfg.n_tokens,
+                 sigma_block_tokens=sblk)
+    if sblk:
+        # one sigma row per block of sblk tokens (each block's own RMS)
+        from lossless_kv_cache_scalar_gb300 import calibrate_sigma
+        w["sigma"] = calibrate_sigma(lay, w["kv"], w["mu"], sblk)
     coder = Coder(lay)
     bits, offs = coder.encode(w["kv"], w["mu"], w["sigma"], w["counts"])
     ref = coder.decode(bits, offs, w["mu"], w["sigma"], w["counts"])
@@ -50,9 +56,11 @@ def test_noalloc_decode_matches_decode_twice(name, kw):
         assert torch.equal(out, w["kv"])
 
 
-def test_noalloc_rejects_layout_beyond_its_scratch():
-    # 100 layers x 2 x 1,024 channels of sigma need 800 KiB + the 256 KiB P_hat table > 1 MiB
-    lay = Layout("bf16", 100, 2, 8, 128, 256)
+@pytest.mark.parametrize("layers,tokens,sblk", [(100, 256, 0), (25, 1024, 256)])
+def test_noalloc_rejects_layout_beyond_its_scratch(layers, tokens, sblk):
+    # 100 planes-pairs x 1,024 channels, or 25 x 4 sigma blocks x 1,024: 800 KiB of
+    # sigma entries + the 256 KiB P_hat table > 1 MiB
+    lay = Layout("bf16", layers, 2, 8, 128, tokens, sigma_block_tokens=sblk)
     dummy = torch.zeros(16, dtype=torch.int64, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     rc = _noalloc(lay, dummy, dummy, dummy, dummy, dummy, dummy, status)
