@@ -52,7 +52,12 @@ constexpr uint32_t kWarpSmem = kRing + kStageWords;   // 32-bit words
 constexpr uint32_t kSmPhi = 0;                                        // Tables
 constexpr uint32_t kSmQt = (sizeof(Tables) + 15u) & ~15u;              // float2[kQuantN + 1]
 constexpr uint32_t kSmT8 = (kSmQt + 8u * (kQuantN + 1) + 15u) & ~15u;  // Tables8
-constexpr uint32_t kSmRing = (kSmT8 + sizeof(Tables8) + 15u) & ~15u;   // uint32 [warps][kRing]
+// w_h P_hat at every 32nd code order with its slope, float2[kPcN + 1]: the
+// estimates' P_hat (interpolated; the exact test reads the exact table)
+constexpr uint32_t kPcShift = 5;
+constexpr uint32_t kPcN = 65536u >> kPcShift;
+constexpr uint32_t kSmPc = (kSmT8 + sizeof(Tables8) + 15u) & ~15u;
+constexpr uint32_t kSmRing = (kSmPc + 8u * (kPcN + 1) + 15u) & ~15u;   // uint32 [warps][kRing]
 template <uint32_t DT>
 constexpr uint32_t dec_smem() { return kSmRing + DecShape<DT>::warps * kWarpSmem * 4u; }
 static_assert(dec_smem<SKV_BF16>() <= 227u * 1024u && dec_smem<SKV_E4M3>() <= 227u * 1024u,
@@ -155,6 +160,36 @@ __device__ __forceinline__ const float2 *dqt() {
     return reinterpret_cast<const float2 *>(skv_dec_smem + kSmQt);
 }
 
+// Stage the per-call tables every CTA of the decoder (or of the search check)
+// reads: the Phi pairs, the quantile table, (e4m3) the code tables and (bf16)
+// the estimates' coarse P_hat table.
+template <uint32_t DT>
+__device__ void stage_decoder_tables(const float *qt_g, const uint32_t *phat, uint32_t w_h) {
+    float *qt = reinterpret_cast<float *>(skv_dec_smem + kSmQt);
+    for (uint32_t i = threadIdx.x; i < kQuantFloats; i += blockDim.x) qt[i] = qt_g[i];
+    if (DT == SKV_BF16) {
+        float2 *pc = reinterpret_cast<float2 *>(skv_dec_smem + kSmPc);
+        for (uint32_t i = threadIdx.x; i <= kPcN; i += blockDim.x) {
+            const uint32_t p0 = w_h ? phat[i << kPcShift] : 0u;
+            const uint32_t p1 = (w_h && i < kPcN) ? phat[(i + 1) << kPcShift] : p0;
+            pc[i] = make_float2((float)w_h * (float)p0, (float)w_h * (float)(p1 - p0) * (1.0f / (1u << kPcShift)));
+        }
+    }
+    stage_tables<DT>(*reinterpret_cast<Tables *>(skv_dec_smem + kSmPhi),
+                     *reinterpret_cast<Tables8 *>(skv_dec_smem + kSmT8), phat);
+}
+
+// w_h P_hat(o) for the estimates only: bf16 interpolated in the coarse table
+// (the estimate is as good as with the exact value), e4m3 exact from its table.
+template <uint32_t DT>
+__device__ __forceinline__ float phat_est(const DecArgs &a, uint32_t o) {
+    if (DT == SKV_BF16) {
+        const float2 e = reinterpret_cast<const float2 *>(skv_dec_smem + kSmPc)[o >> kPcShift];
+        return fmaf((float)(o & ((1u << kPcShift) - 1u)), e.y, e.x);
+    }
+    return (float)(a.g.w_h * dtab8()->phat[o]);
+}
+
 // C(o) and P_hat(o) for the decoder: with EP (bf16 and a full workspace) from
 // the per-call (edge bits, P_hat) pair table, else from the code bits and the
 // P_hat table. Both give the same values.
@@ -184,7 +219,7 @@ template <> __device__ __forceinline__ uint32_t nearest_ord<SKV_E4M3>(float x) {
 }
 
 // One estimate of the code of slot s, with p_hat's share and the floor term
-// taken at o_ref (ph_ref = P_hat(o_ref)). far: the quantile is within 2^-40 of
+// taken at o_ref (ph = w_h P_hat(o_ref)). far: the quantile is within 2^-40 of
 // an end, where only p_hat and the floor hold mass; below: nearer the low end.
 // Besides the code's order it keeps what a second pass reuses: the quantile gt,
 // its log2, the table's z there and the table cell's slope.
@@ -195,11 +230,10 @@ struct Estimate {
 };
 template <uint32_t DT>
 __device__ __forceinline__ Estimate estimate(const DecArgs &a, float kS, float inv_total, uint32_t s,
-                                             uint32_t o_ref, uint32_t ph_ref, float mu, float sigma) {
+                                             uint32_t o_ref, float ph, float mu, float sigma) {
     using K = Codes<DT>;
     constexpr int MN = (int)((1u << K::m) - K::N);
     Estimate r;
-    const float ph = (float)(a.g.w_h * ph_ref);
     const float ph_top = (float)(a.g.w_h << 24) - ph;
     // the quantile of the Gaussian part, measured from whichever end is nearer
     const int d = (int)s - (int)o_ref;
@@ -228,10 +262,10 @@ __device__ __forceinline__ Estimate estimate(const DecArgs &a, float kS, float i
 // first estimate o1 move the quantile by D; the new quantile's log2 moves z
 // along the first pass's table cell (taken at mu's code, the first estimate
 // errs outwards on the true code's side, so its side is kept).
-__device__ __forceinline__ uint32_t estimate2(const DecArgs &a, float kS, float inv_total, const Estimate &e1,
-                                              uint32_t o_ref, uint32_t ph_ref, uint32_t o1, uint32_t ph1,
-                                              float mu, float sigma, bool &far) {
-    const float D = fmaf((float)(int)(o1 - o_ref), kS, (float)((int)a.g.w_h * (int)(ph1 - ph_ref)));
+__device__ __forceinline__ uint32_t estimate2(float kS, float inv_total, const Estimate &e1, uint32_t o_ref,
+                                              float ph_ref, uint32_t o1, float ph1, float mu, float sigma,
+                                              bool &far) {
+    const float D = fmaf((float)(int)(o1 - o_ref), kS, ph1 - ph_ref);
     const float gt = fmaf(e1.below ? -D : D, inv_total, e1.gt);
     far = !(gt >= 9.094947e-13f);
     float lg;
@@ -300,7 +334,7 @@ __device__ __forceinline__ uint32_t saturated_inverse(const DecArgs &a, uint32_t
 template <uint32_t DT, bool EP>
 __device__ __forceinline__ uint32_t find_symbol(const DecArgs &a, float kS, float inv_total,
                                                 uint32_t s, float mu, float rs, uint32_t o_mu,
-                                                uint32_t ph_mu, uint32_t &c_out, uint32_t &f_out) {
+                                                float ph_mu, uint32_t &c_out, uint32_t &f_out) {
     using K = Codes<DT>;
     const Weights w{a.g.w_n, a.g.w_w, a.g.w_h};
     uint32_t o = o_mu;
@@ -320,8 +354,7 @@ __device__ __forceinline__ uint32_t find_symbol(const DecArgs &a, float kS, floa
         if (DT == SKV_BF16 && !far) {
             // second pass (bf16 only: e4m3's eight codes per binade leave the
             // first estimate as good as a second one)
-            const uint32_t ph1 = w.h ? phat_dec<DT, EP>(a, o) : 0u;
-            o = estimate2(a, kS, inv_total, e1, o_mu, ph_mu, o, ph1, mu, sigma, far);
+            o = estimate2(kS, inv_total, e1, o_mu, ph_mu, o, phat_est<DT>(a, o), mu, sigma, far);
             // only p_hat holds mass this far out: the saturated inverse gives the code
             if (far) o = saturated_inverse<DT>(a, s, below ? 0u : (w.n + w.w) << 24);
         } else if (far) {
@@ -498,7 +531,7 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
                     mu = DT == SKV_E4M3 ? dtab8()->value[mc] : K::value(mc);
                     rs = __ldg(rse + pi);
                     const uint32_t om = K::ord(mc);
-                    const uint32_t ph = g.w_h ? phat_dec<DT, EP>(a, om) : 0u;
+                    const float ph = phat_est<DT>(a, om);
                     slot = (uint32_t)x & (M - 1u);
                     o = find_symbol<DT, EP>(a, kS, inv_total, slot, mu, rs, om, ph, c, f);
                     miss = slot - c >= f;    // c, slot < 2^24: c > slot wraps far above any f
@@ -557,12 +590,7 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
 template <uint32_t DT, bool EP>
 __global__ void __launch_bounds__(DecShape<DT>::warps * 32, DecShape<DT>::ctas) decode_kernel(const DecArgs a) {
     constexpr int kDecWarps = DecShape<DT>::warps;
-    {
-        float *qt = reinterpret_cast<float *>(skv_dec_smem + kSmQt);
-        for (uint32_t i = threadIdx.x; i < kQuantFloats; i += blockDim.x) qt[i] = a.qt[i];
-        stage_tables<DT>(*reinterpret_cast<Tables *>(skv_dec_smem + kSmPhi),
-                         *reinterpret_cast<Tables8 *>(skv_dec_smem + kSmT8), a.phat);
-    }
+    stage_decoder_tables<DT>(a.qt, a.phat, a.g.w_h);
     const uint32_t warp = threadIdx.x >> 5;
     uint32_t *ring = reinterpret_cast<uint32_t *>(skv_dec_smem + kSmRing) + warp * kWarpSmem;
     const uint64_t n_groups = a.n_units * a.g.G;
@@ -581,12 +609,7 @@ template <uint32_t DT, bool EP>
 __global__ void __launch_bounds__(256) search_kernel(const SearchArgs sa) {
     using K = Codes<DT>;
     constexpr uint32_t M = 1u << K::m;
-    {
-        float *qt = reinterpret_cast<float *>(skv_dec_smem + kSmQt);
-        for (uint32_t i = threadIdx.x; i < kQuantFloats; i += blockDim.x) qt[i] = sa.qt[i];
-        stage_tables<DT>(*reinterpret_cast<Tables *>(skv_dec_smem + kSmPhi),
-                         *reinterpret_cast<Tables8 *>(skv_dec_smem + kSmT8), sa.phat);
-    }
+    stage_decoder_tables<DT>(sa.qt, sa.phat, sa.g.w_h);
     DecArgs a{};
     a.g = sa.g;
     a.phat = sa.phat;
@@ -614,7 +637,7 @@ __global__ void __launch_bounds__(256) search_kernel(const SearchArgs sa) {
         const float mu = fin ? K::value(mc) : 0.0f;
         const uint32_t slot = active ? sa.slots[q] & (M - 1u) : 0u;
         const uint32_t o_mu = K::ord(fin ? mc : 0u);
-        const uint32_t ph = g.w_h ? phat_dec<DT, EP>(a, o_mu) : 0u;
+        const float ph = phat_est<DT>(a, o_mu);
         uint32_t o = 0, c = 0, f = 1;
         bool miss = false;
         if (active) {
