@@ -536,8 +536,24 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
                     o = find_symbol<DT, EP>(a, kS, inv_total, slot, mu, rs, om, ph, c, f);
                     miss = slot - c >= f;    // c, slot < 2^24: c > slot wraps far above any f
                 }
-                // misses are resolved by the whole warp, one lane at a time
+                // misses: first one secant step by every missing lane at once (the
+                // exact C(o) and f(o) say how many codes away the slot lies), then
+                // the whole warp for each lane still missing, one lane at a time
                 uint32_t pending = __ballot_sync(0xFFFFFFFFu, miss);
+                if (pending) {
+                    if (miss) {
+                        float rf;
+                        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rf) : "f"((float)f));
+                        int dlt = __float2int_rd((float)(int)(slot - c) * rf);
+                        dlt = (int)(slot - c) < 0 ? min(dlt, -1) : max(dlt, 1);
+                        const uint32_t o2 = (uint32_t)min(max((int)o + dlt, 0), (int)K::N - 1);
+                        const uint32_t c2 = cdf_dec<DT, EP>(a, o2, mu, rs);
+                        const uint32_t f2 = cdf_dec<DT, EP>(a, o2 + 1u, mu, rs) - c2;
+                        o = o2; c = c2; f = f2;
+                        miss = slot - c >= f;
+                    }
+                    pending = __ballot_sync(0xFFFFFFFFu, miss);
+                }
                 while (pending) {
                     const uint32_t Lm = __ffs(pending) - 1u;
                     pending &= pending - 1u;
