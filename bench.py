@@ -160,6 +160,36 @@ def cpu_oracle_run(cfg, sample_chunks: int, nthreads: int, seconds_hint: float =
     return nbytes, dt, desc
 
 
+def rate_sample(w, offsets, lay, layers: int = 4):
+    """Coded bits over the ideal cross-entropy (the CPU oracle's real-valued
+    mixture, libm) on a sample of the workload: the first 256-token page of K
+    and V in `layers` evenly spaced layers, coded bits from the GPU stream's
+    offsets. The rate bound of the method asks for at most 1.01."""
+    from oracle import oracle as O
+    L, T = w["kv"].shape[0], w["kv"].shape[2]
+    tc = min(lay.tokens_per_chunk, T)
+    pages = -(-T // lay.tokens_per_chunk)
+    offs = offsets.cpu().numpy().astype(np.int64)
+    counts = w["counts"].cpu().numpy().astype(np.uint64)
+    coded = ideal = 0.0
+    picked = sorted(set(int(i * L / layers) for i in range(layers)))
+    for l in picked:
+        sub = O.Layout(O.BF16 if lay.dtype == "bf16" else O.E4M3, 1, lay.n_kv, lay.n_heads, lay.head_dim, tc,
+                       tokens_per_chunk=lay.tokens_per_chunk, streams_per_chunk=lay.streams_per_chunk,
+                       w_n=lay.weights[0], w_w=lay.weights[1], w_h=lay.weights[2])
+        kv = w["kv"][l:l + 1, :, :tc].cpu().numpy()
+        mu = w["mu"][l:l + 1, :, :tc].cpu().numpy()
+        sig = w["sigma"][l:l + 1].cpu().numpy()
+        if lay.sigma_block_tokens:
+            sig = sig[:, :, :1]
+        ideal += O.ideal_bits(sub, kv, mu, sig.reshape(1, lay.n_kv, lay.n_heads, lay.head_dim), counts)
+        for kvi in range(lay.n_kv):
+            k = (l * lay.n_kv + kvi) * pages
+            coded += 8.0 * (offs[k + 1] - offs[k])
+    return {"bits_over_ideal": coded / ideal, "sample": f"page 0 of K and V in layers {picked}",
+            "ideal": "sum of -log2 q over the sample, q the real-valued mixture over each code's interval"}
+
+
 def cpu_table(single_chunks: int = 8, parallel_chunks: int = 64):
     """The CPU oracle on every workload recipe: encode + decode throughput
     (GB/s of uncompressed KV) single-threaded and chunk-parallel over all the
@@ -428,6 +458,10 @@ def main():
                    "sample": desc}
           except Exception as e:  # the baseline must not hide the GPU number
             cpu = {"value": None, "unit": "GB/s", "cores": None, "kind": "oracle", "sample": f"failed: {e}"}
+        try:
+            rate = rate_sample(w, offsets, lay)
+        except Exception as e:  # a check beside the number, not the number
+            rate = {"bits_over_ideal": None, "sample": f"failed: {e}"}
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * t_tot / args.steps, "higher_is_better": True,
@@ -442,7 +476,7 @@ def main():
                        "streams_per_chunk": lay.streams_per_chunk, "weights": list(lay.weights),
                        "sigma_block_tokens": lay.sigma_block_tokens,
                        "l2": "inputs 2 x %.1f GB >> 129 MB L2, no flush" % (raw_bytes / 1e9)},
-            "encode_gbs": enc_gbs, "decode_gbs": dec_gbs, "bits_per_scalar": bits,
+            "encode_gbs": enc_gbs, "decode_gbs": dec_gbs, "bits_per_scalar": bits, "rate": rate,
             "compression_ratio": 8.0 * lay.bytes_per_code / bits,
             "sigma_side_bits_per_scalar": sigma_side_bits,
             "roofline": {"bound": "alu", "kernel": dom, "achieved": achieved, "peak": peak_tops,
