@@ -53,6 +53,27 @@ def assert_same_stream(lay: Layout, wd: dict, wh: dict):
     return s, offs, c
 
 
+def slice_chunks(lay: Layout, wd: dict, ks):
+    """The inputs of full-page chunks ks stacked as one layout of len(ks)
+    one-page planes (host numpy): plane i is chunk ks[i], with its own sigma."""
+    P = -(-lay.n_tokens // lay.tokens_per_chunk)
+    kvs, mus, sigs = [], [], []
+    for k in ks:
+        plane, page = divmod(int(k), P)
+        l, kv = divmod(plane, lay.n_kv)
+        t0 = page * lay.tokens_per_chunk
+        assert t0 + lay.tokens_per_chunk <= lay.n_tokens, "full pages only"
+        kvs.append(wd["kv"][l, kv, t0:t0 + lay.tokens_per_chunk])
+        mus.append(wd["mu"][l, kv, t0:t0 + lay.tokens_per_chunk])
+        sigs.append(wd["sigma"][l, kv])
+    sub = Layout(lay.dtype, len(ks), 1, lay.n_heads, lay.head_dim, lay.tokens_per_chunk, lay.tokens_per_chunk,
+                 lay.streams_per_chunk, lay.weights)
+    import torch
+    part = {"kv": torch.stack(kvs)[:, None].contiguous(), "mu": torch.stack(mus)[:, None].contiguous(),
+            "sigma": torch.stack(sigs)[:, None].contiguous(), "counts": wd["counts"]}
+    return sub, host(part)
+
+
 def slice_chunk(lay: Layout, wd: dict, k: int):
     """The inputs of chunk k alone, as a one-chunk layout (host numpy)."""
     P = -(-lay.n_tokens // lay.tokens_per_chunk)

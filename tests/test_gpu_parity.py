@@ -351,15 +351,17 @@ def test_full_size_sampled(name):
     c.check_status("decode")
     assert torch.equal(back, wd["kv"])
     del back
-    rng = np.random.default_rng(zlib.crc32(name.encode()))   # fixed per workload
+    # 64 chunks byte-compared with the oracle: the first and last, and 62 drawn
+    # (fixed seed per workload) from every layer, K and V alike
+    rng = np.random.default_rng(zlib.crc32(name.encode()))
     n = lay.n_chunks
-    ks = sorted(set([0, n - 1] + rng.integers(0, n, 3).tolist()))
+    ks = sorted(set([0, n - 1] + rng.choice(n, 62, replace=False).tolist()))
     offs_h = offs.cpu().numpy()
-    for k in ks:
-        sub, part = H.slice_chunk(lay, wd, k)
-        so, oo = O.encode(H.o_layout(sub), part["kv"], part["mu"], part["sigma"], part["counts"])
+    sub, part = H.slice_chunks(lay, wd, ks)
+    so, oo = O.encode(H.o_layout(sub), part["kv"], part["mu"], part["sigma"], part["counts"])
+    for i, k in enumerate(ks):
         got = s[int(offs_h[k]):int(offs_h[k + 1])].cpu().numpy()
-        assert np.array_equal(got, so), (name, k)
+        assert np.array_equal(got, so[int(oo[i]):int(oo[i + 1])]), (name, k)
     bits = 8.0 * float(offs_h[-1]) / lay.n_elems
     assert bits < (7.0 if lay.dtype == "bf16" else 4.0), bits
 
