@@ -17,11 +17,15 @@
 // (w_n + w_w); a table in t = -log2(min(g, 1 - g)) gives z = G^-1(g); and
 // mu + z sigma rounded to the code grid is the estimate (a code owns the reals
 // that round to it, SKV v1 format §2). A first pass takes the reference at
-// mu's own code, a second (bf16) at the first estimate. A far outlier that only
+// mu's own code, a second (bf16) at the first estimate; both take P_hat from a
+// coarse shared-memory table (every 32nd order, interpolated), which leaves
+// their miss rate as it is with the exact P_hat. A far outlier that only
 // p_hat explains (both Gaussians saturated, so C is a mu-independent function
-// of o) is read from per-call inverse tables instead. When the test fails,
-// the whole warp searches for that lane's code together (cooperative_search).
-// Search aids change speed only; the decoded codes are fixed by the exact test.
+// of o) is read from per-call inverse tables instead. When the test fails, the
+// lane first takes one secant step from the exact C(o) and f(o) (all missing
+// lanes at once); a lane still missing is searched by the whole warp together
+// (cooperative_search). Search aids change speed only; the decoded codes are
+// fixed by the exact test.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -33,9 +37,10 @@
 namespace skv {
 
 // CTA shape: one persistent CTA of 32 warps per SM for both code types. The
-// Phi pairs, quantile table and (e4m3) code tables are staged once per SM;
-// for bf16 the rest of the SM's L1 caches the (edge, P_hat) pair table. (Four
-// 8-warp CTAs per SM measured 4% slower for e4m3 and 8% for bf16.)
+// Phi pairs, quantile table, coarse P_hat table and (e4m3) code tables are
+// staged once per SM; for bf16 the rest of the SM's L1 caches the (edge,
+// P_hat) pair table the exact test reads. (Four 8-warp CTAs per SM measured 4%
+// slower for e4m3 and 8% for bf16.)
 template <uint32_t DT> struct DecShape { static constexpr int warps = 32, ctas = 1; };
 static_assert(DecShape<SKV_BF16>::warps * DecShape<SKV_BF16>::ctas == (int)kDecResidentWarps &&
               DecShape<SKV_E4M3>::warps * DecShape<SKV_E4M3>::ctas == (int)kDecResidentWarps,
