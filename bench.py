@@ -86,21 +86,38 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampling of SM clocks and throttle reasons. Started before the
+    warm-up (so that it is sampling once the timed region begins); only the
+    samples whose timestamps fall inside the timed region's host window
+    (mark_start .. mark_end) are kept."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.path = tempfile.mktemp(prefix="skv_clocks_", suffix=".csv")
         self.proc = None
+        self.t0 = self.t1 = None
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200", "-i", str(gpu_index)], stdout=self.fh,
+                                          "-lms", "100", "-i", str(gpu_index)], stdout=self.fh,
                                          stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+        if self.proc is not None:
+            import atexit
+            atexit.register(self._end)
+
+    def _end(self):
+        if self.proc is not None and self.proc.poll() is None:
+            self.proc.kill()
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def stop(self) -> dict:
         if self.proc is None:
@@ -111,25 +128,30 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        sm, smax, reasons = [], [], set()
+        import datetime
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as fh:
             for line in fh:
                 p = [x.strip() for x in line.split(",")]
-                if len(p) < 9:
+                if len(p) < 10:
                     continue
                 try:
-                    sm.append(float(p[1]))
-                    smax.append(float(p[2]))
+                    ts = datetime.datetime.strptime(p[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(p[2]), float(p[3]), {n for n, v in zip(names, p[6:10])
+                                                                 if v.lower() == "active"}))
                 except ValueError:
                     continue
-                for n, v in zip(names, p[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(n)
         os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+        inside = [r for r in rows if self.t0 is not None and self.t1 is not None and self.t0 <= r[0] <= self.t1]
+        window = "timed region"
+        if not inside:      # a region shorter than the sampling period: the nearest sample after its start
+            after = [r for r in rows if self.t0 is None or r[0] >= self.t0]
+            inside, window = after[:1], "first sample after the timed region began"
+        return {"sm_mhz": statistics.median(r[1] for r in inside) if inside else None,
+                "sm_max_mhz": max(r[2] for r in inside) if inside else None,
+                "samples": len(inside), "window": window,
+                "reasons": sorted(set().union(*(r[3] for r in inside))) if inside else []}
 
 
 def _dist():
@@ -227,7 +249,7 @@ def run_reference(args, cfg):
     gbs = total_b / total_t / 1e9
     line = {"metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32/u64 int + f32",
+            "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "u32/u64 int + f32",
             "data": "synthetic", "impl": "reference",
             "config": {"workload": cfg.name, "shape": [cfg.n_layers, cfg.n_kv, cfg.n_tokens, cfg.n_heads,
                                                        cfg.head_dim],
@@ -245,7 +267,7 @@ METRIC = "KV encode+decode GB/s (uncompressed bytes) on GB300"
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", default="qwen3_8b")
     ap.add_argument("--impl", default="skv", choices=["skv", "reference"])
@@ -332,6 +354,7 @@ def main():
         coder.encode_into(w["kv"], w["mu"], w["sigma"], w["counts"], out, offsets, s)
         coder.decode_into(out, offsets, w["mu"], w["sigma"], w["counts"], back, s)
 
+    sampler = ClockSampler(local) if rank == 0 else None
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             step(stream)
@@ -346,8 +369,9 @@ def main():
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    sampler = ClockSampler(local) if rank == 0 else None
     barrier()
+    if sampler:
+        sampler.mark_start()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     with torch.cuda.stream(stream):
         for i in range(args.steps):
@@ -357,6 +381,8 @@ def main():
             coder.decode_into(out, offsets, w["mu"], w["sigma"], w["counts"], back, stream)
             ev[i][2].record(stream)
     barrier()
+    if sampler:
+        sampler.mark_end()
     clocks = sampler.stop() if sampler else {}
     coder.check_status("timed", stream)
     t_enc = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3
@@ -758,7 +784,7 @@ def e2e_run(coder, w, lay, args, dev, total_bytes):
     offs_h = torch.empty(lay.n_chunks + 1, dtype=torch.int64).pin_memory()
     back_h = torch.empty(kv_h.shape, dtype=kv_h.dtype).pin_memory()
     stream = torch.cuda.Stream(device=dev)
-    steps = max(1, min(args.steps, 3))
+    steps = max(1, min(args.steps, 5))
     t_enc, t_dec = [], []
     with torch.cuda.stream(stream):
         for i in range(1 + steps):
