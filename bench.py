@@ -95,16 +95,18 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
-        self.path = tempfile.mktemp(prefix="skv_clocks_", suffix=".csv")
+        fd, self.path = tempfile.mkstemp(prefix="skv_clocks_", suffix=".csv")
+        self.fh = os.fdopen(fd, "w")
         self.proc = None
         self.t0 = self.t1 = None
         try:
-            self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                                           "-lms", "100", "-i", str(gpu_index)], stdout=self.fh,
                                          stderr=subprocess.DEVNULL)
-        except (OSError, FileNotFoundError):
+        except OSError:
             self.proc = None
+            self.fh.close()
+            os.unlink(self.path)
         if self.proc is not None:
             import atexit
             atexit.register(self._end)
