@@ -37,9 +37,9 @@
 namespace skv {
 
 // CTA shape: one persistent CTA of 32 warps per SM for both code types. The
-// Phi pairs, quantile table, coarse P_hat table and (e4m3) code tables are
-// staged once per SM; for bf16 the rest of the SM's L1 caches the (edge,
-// P_hat) pair table the exact test reads. (Four 8-warp CTAs per SM measured 4%
+// Phi pairs, quantile table, (bf16) coarse P_hat table and (e4m3) lane-sliced
+// code tables are staged once per SM; for bf16 the rest of the SM's L1 caches
+// the (edge, P_hat) pair table the exact test reads. (Four 8-warp CTAs per SM measured 4%
 // slower for e4m3 and 8% for bf16.)
 template <uint32_t DT> struct DecShape { static constexpr int warps = 32, ctas = 1; };
 static_assert(DecShape<SKV_BF16>::warps * DecShape<SKV_BF16>::ctas == (int)kDecResidentWarps &&
@@ -53,18 +53,28 @@ constexpr uint32_t kBlock = 64;        // words per cp.async block (16 B per lan
 constexpr uint32_t kStageWords = 4u * 32u;
 constexpr uint32_t kWarpSmem = kRing + kStageWords;   // 32-bit words
 
-// dynamic shared memory layout (bytes)
+// dynamic shared memory layout (bytes): Phi pairs and quantile table, then
+// per code type its own tables, then the warps' word rings
 constexpr uint32_t kSmPhi = 0;                                        // Tables
 constexpr uint32_t kSmQt = (sizeof(Tables) + 15u) & ~15u;              // float2[kQuantN + 1]
-constexpr uint32_t kSmT8 = (kSmQt + 8u * (kQuantN + 1) + 15u) & ~15u;  // Tables8
-// w_h P_hat at every 32nd code order with its slope, float2[kPcN + 1]: the
-// estimates' P_hat (interpolated; the exact test reads the exact table)
+constexpr uint32_t kSmCode = (kSmQt + 8u * (kQuantN + 1) + 15u) & ~15u;
+// bf16: w_h P_hat at every 32nd code order with its slope, float2[kPcN + 1]:
+// the estimates' P_hat (interpolated; the exact test reads the exact table)
 constexpr uint32_t kPcShift = 5;
 constexpr uint32_t kPcN = 65536u >> kPcShift;
-constexpr uint32_t kSmPc = (kSmT8 + sizeof(Tables8) + 15u) & ~15u;
-constexpr uint32_t kSmRing = (kSmPc + 8u * (kPcN + 1) + 15u) & ~15u;   // uint32 [warps][kRing]
+constexpr uint32_t kSmPc = kSmCode;
+// e4m3: the code tables (edge, P_hat, value of every code) lane-sliced, entry
+// i of lane l at word 32 i + l: the 32 lanes of a warp, each looking up its
+// own code, hit 32 distinct banks (a shared copy measured 6% slower, its bank
+// conflicts keeping the shared-memory pipe busy)
+constexpr uint32_t kSlEdge = 0, kSlPhat = 257u * 32u, kSlValue = 2u * 257u * 32u;
+constexpr uint32_t kSlWords = kSlValue + 256u * 32u;
 template <uint32_t DT>
-constexpr uint32_t dec_smem() { return kSmRing + DecShape<DT>::warps * kWarpSmem * 4u; }
+__host__ __device__ constexpr uint32_t sm_ring() {           // uint32 [warps][kWarpSmem]
+    return DT == SKV_E4M3 ? ((kSmCode + 4u * kSlWords + 15u) & ~15u) : ((kSmPc + 8u * (kPcN + 1) + 15u) & ~15u);
+}
+template <uint32_t DT>
+constexpr uint32_t dec_smem() { return sm_ring<DT>() + DecShape<DT>::warps * kWarpSmem * 4u; }
 static_assert(dec_smem<SKV_BF16>() <= 227u * 1024u && dec_smem<SKV_E4M3>() <= 227u * 1024u,
               "decoder shared memory above the per-CTA limit");
 
@@ -158,9 +168,13 @@ extern __shared__ __align__(16) uint8_t skv_dec_smem[];
 __device__ __forceinline__ const Tables &dtab() {
     return *reinterpret_cast<const Tables *>(skv_dec_smem + kSmPhi);
 }
-__device__ __forceinline__ const Tables8 *dtab8() {
-    return reinterpret_cast<const Tables8 *>(skv_dec_smem + kSmT8);
+// this lane's slice of an e4m3 code table
+__device__ __forceinline__ const uint32_t *dsl(uint32_t base) {
+    return reinterpret_cast<const uint32_t *>(skv_dec_smem + kSmCode) + base + (threadIdx.x & 31u);
 }
+__device__ __forceinline__ float sl_edge(uint32_t o) { return __uint_as_float(dsl(kSlEdge)[o << 5]); }
+__device__ __forceinline__ uint32_t sl_phat(uint32_t o) { return dsl(kSlPhat)[o << 5]; }
+__device__ __forceinline__ float sl_value(uint32_t c) { return __uint_as_float(dsl(kSlValue)[c << 5]); }
 __device__ __forceinline__ const float2 *dqt() {
     return reinterpret_cast<const float2 *>(skv_dec_smem + kSmQt);
 }
@@ -180,8 +194,16 @@ __device__ void stage_decoder_tables(const float *qt_g, const uint32_t *phat, ui
             pc[i] = make_float2((float)w_h * (float)p0, (float)w_h * (float)(p1 - p0) * (1.0f / (1u << kPcShift)));
         }
     }
-    stage_tables<DT>(*reinterpret_cast<Tables *>(skv_dec_smem + kSmPhi),
-                     *reinterpret_cast<Tables8 *>(skv_dec_smem + kSmT8), phat);
+    if (DT == SKV_E4M3) {
+        uint32_t *sl = reinterpret_cast<uint32_t *>(skv_dec_smem + kSmCode);
+        for (uint32_t i = threadIdx.x; i < 257u * 32u; i += blockDim.x) {
+            sl[kSlEdge + i] = __float_as_uint(edge_from_values<SKV_E4M3>(i >> 5));
+            sl[kSlPhat + i] = phat[i >> 5];
+            if (i < 256u * 32u) sl[kSlValue + i] = __float_as_uint(Codes<SKV_E4M3>::value(i >> 5));
+        }
+    }
+    stage_phi(*reinterpret_cast<Tables *>(skv_dec_smem + kSmPhi));
+    __syncthreads();
 }
 
 // w_h P_hat(o) for the estimates only: bf16 interpolated in the coarse table
@@ -192,22 +214,25 @@ __device__ __forceinline__ float phat_est(const DecArgs &a, uint32_t o) {
         const float2 e = reinterpret_cast<const float2 *>(skv_dec_smem + kSmPc)[o >> kPcShift];
         return fmaf((float)(o & ((1u << kPcShift) - 1u)), e.y, e.x);
     }
-    return (float)(a.g.w_h * dtab8()->phat[o]);
+    return (float)(a.g.w_h * sl_phat(o));
 }
 
 // C(o) and P_hat(o) for the decoder: with EP (bf16 and a full workspace) from
-// the per-call (edge bits, P_hat) pair table, else from the code bits and the
-// P_hat table. Both give the same values.
+// the per-call (edge bits, P_hat) pair table, else (bf16) from the code bits
+// and the P_hat table, or (e4m3) from the lane-sliced code tables. All give
+// the same values.
 template <uint32_t DT, bool EP>
 __device__ __forceinline__ uint32_t cdf_dec(const DecArgs &a, uint32_t o, float mu, float rs) {
     const Weights w{a.g.w_n, a.g.w_w, a.g.w_h};
     if (EP) return cdf_ep(dtab(), w, a.ep, o, mu, rs);
-    return cdf<DT>(dtab(), dtab8(), w, a.phat, o, mu, rs);
+    if (DT == SKV_E4M3) return cdf_from<SKV_E4M3>(dtab(), w, sl_edge(o), sl_phat(o), o, mu, rs);
+    return cdf<SKV_BF16>(dtab(), nullptr, w, a.phat, o, mu, rs);
 }
 template <uint32_t DT, bool EP>
 __device__ __forceinline__ uint32_t phat_dec(const DecArgs &a, uint32_t o) {
     if (EP) return __ldg(&a.ep[o].y);
-    return Codes<DT>::phat(dtab8(), a.phat, o);
+    if (DT == SKV_E4M3) return sl_phat(o);
+    return Codes<SKV_BF16>::phat(nullptr, a.phat, o);
 }
 
 // Round a value to the nearest code (ties to even), clamped to the finite codes.
@@ -533,7 +558,7 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
                 if (active) {
                     const uint32_t mc = BITS == 16 ? (uint32_t)reinterpret_cast<const uint16_t *>(sw)[pi]
                                                    : (uint32_t)reinterpret_cast<const uint8_t *>(sw)[pi];
-                    mu = DT == SKV_E4M3 ? dtab8()->value[mc] : K::value(mc);
+                    mu = DT == SKV_E4M3 ? sl_value(mc) : K::value(mc);
                     rs = __ldg(rse + pi);
                     const uint32_t om = K::ord(mc);
                     const float ph = phat_est<DT>(a, om);
@@ -613,7 +638,7 @@ __global__ void __launch_bounds__(DecShape<DT>::warps * 32, DecShape<DT>::ctas) 
     constexpr int kDecWarps = DecShape<DT>::warps;
     stage_decoder_tables<DT>(a.qt, a.phat, a.g.w_h);
     const uint32_t warp = threadIdx.x >> 5;
-    uint32_t *ring = reinterpret_cast<uint32_t *>(skv_dec_smem + kSmRing) + warp * kWarpSmem;
+    uint32_t *ring = reinterpret_cast<uint32_t *>(skv_dec_smem + sm_ring<DT>()) + warp * kWarpSmem;
     const uint64_t n_groups = a.n_units * a.g.G;
     for (uint64_t gid = (uint64_t)warp * gridDim.x + blockIdx.x; gid < n_groups;
          gid += (uint64_t)gridDim.x * kDecWarps) {
@@ -685,7 +710,8 @@ int launch_search_eval(const SearchArgs &sa, cudaStream_t st) {
     if (sa.n == 0) return 0;
     uint64_t blocks = (sa.n + 255u) / 256u;
     if (blocks > 4096u) blocks = 4096u;
-    const uint32_t smem = kSmRing;                    // tables and quantiles, no word rings
+    // the tables, no word rings
+    const uint32_t smem = sa.g.dtype == SKV_BF16 ? sm_ring<SKV_BF16>() : sm_ring<SKV_E4M3>();
     if (sa.g.dtype == SKV_BF16) {
         if (sa.ep) {
             if (cudaFuncSetAttribute(search_kernel<SKV_BF16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,

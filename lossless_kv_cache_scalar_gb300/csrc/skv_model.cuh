@@ -131,9 +131,9 @@ __device__ float edge_from_values(uint32_t o) {
     return __fadd_rn(__fmul_rn(0.5f, a), __fmul_rn(0.5f, b));
 }
 
-// Stage the Phi pairs (and, for e4m3, the edges and P_hat) into shared memory.
-template <uint32_t DT, bool WIDE>
-__device__ void stage_tables(PhiTables<WIDE> &t, Tables8 &t8, const uint32_t *__restrict__ phat) {
+// Stage the Phi pairs into shared memory (no barrier).
+template <bool WIDE>
+__device__ void stage_phi(PhiTables<WIDE> &t) {
     constexpr int off = PhiTables<WIDE>::kCenter - 2048;     // entry of T[0]
     for (uint32_t i = threadIdx.x; i < PhiTables<WIDE>::kEntries; i += blockDim.x) {
         const int j = (int)i - off;
@@ -143,6 +143,12 @@ __device__ void stage_tables(PhiTables<WIDE> &t, Tables8 &t8, const uint32_t *__
         else e = make_uint2(kPhiQ24[j], kPhiQ24[j + 1] - kPhiQ24[j]);
         t.phi[i] = e;
     }
+}
+
+// Stage the Phi pairs (and, for e4m3, the edges and P_hat) into shared memory.
+template <uint32_t DT, bool WIDE>
+__device__ void stage_tables(PhiTables<WIDE> &t, Tables8 &t8, const uint32_t *__restrict__ phat) {
+    stage_phi(t);
     if (DT == SKV_E4M3) {
         for (uint32_t o = threadIdx.x; o <= 256u; o += blockDim.x) {
             t8.edge[o] = edge_from_values<SKV_E4M3>(o);
