@@ -63,15 +63,12 @@ constexpr uint32_t kSmCode = (kSmQt + 8u * (kQuantN + 1) + 15u) & ~15u;
 constexpr uint32_t kPcShift = 5;
 constexpr uint32_t kPcN = 65536u >> kPcShift;
 constexpr uint32_t kSmPc = kSmCode;
-// e4m3: the code tables (edge, P_hat, value of every code) lane-sliced, entry
-// i of lane l at word 32 i + l: the 32 lanes of a warp, each looking up its
-// own code, hit 32 distinct banks (a shared copy measured 6% slower, its bank
-// conflicts keeping the shared-memory pipe busy)
-constexpr uint32_t kSlEdge = 0, kSlPhat = 257u * 32u, kSlValue = 2u * 257u * 32u;
-constexpr uint32_t kSlWords = kSlValue + 256u * 32u;
+// e4m3: the lane-sliced code tables (Sliced8; a single shared copy measured
+// 6% slower, its bank conflicts keeping the shared-memory pipe busy)
 template <uint32_t DT>
 __host__ __device__ constexpr uint32_t sm_ring() {           // uint32 [warps][kWarpSmem]
-    return DT == SKV_E4M3 ? ((kSmCode + 4u * kSlWords + 15u) & ~15u) : ((kSmPc + 8u * (kPcN + 1) + 15u) & ~15u);
+    return DT == SKV_E4M3 ? ((kSmCode + 4u * Sliced8::kWords + 15u) & ~15u)
+                          : ((kSmPc + 8u * (kPcN + 1) + 15u) & ~15u);
 }
 template <uint32_t DT>
 constexpr uint32_t dec_smem() { return sm_ring<DT>() + DecShape<DT>::warps * kWarpSmem * 4u; }
@@ -168,13 +165,15 @@ extern __shared__ __align__(16) uint8_t skv_dec_smem[];
 __device__ __forceinline__ const Tables &dtab() {
     return *reinterpret_cast<const Tables *>(skv_dec_smem + kSmPhi);
 }
-// this lane's slice of an e4m3 code table
-__device__ __forceinline__ const uint32_t *dsl(uint32_t base) {
-    return reinterpret_cast<const uint32_t *>(skv_dec_smem + kSmCode) + base + (threadIdx.x & 31u);
+// this lane's entries of the lane-sliced e4m3 code tables (Sliced8's layout),
+// addressed from the shared array itself so that the loads stay shared-memory
+// loads (through a Sliced8 built from a plain pointer the decoder ran 2% slower)
+__device__ __forceinline__ const uint32_t *dsl(uint32_t table) {
+    return reinterpret_cast<const uint32_t *>(skv_dec_smem + kSmCode) + table + (threadIdx.x & 31u);
 }
-__device__ __forceinline__ float sl_edge(uint32_t o) { return __uint_as_float(dsl(kSlEdge)[o << 5]); }
-__device__ __forceinline__ uint32_t sl_phat(uint32_t o) { return dsl(kSlPhat)[o << 5]; }
-__device__ __forceinline__ float sl_value(uint32_t c) { return __uint_as_float(dsl(kSlValue)[c << 5]); }
+__device__ __forceinline__ float sl_edge(uint32_t o) { return __uint_as_float(dsl(Sliced8::kEdge)[o << 5]); }
+__device__ __forceinline__ uint32_t sl_phat(uint32_t o) { return dsl(Sliced8::kPhat)[o << 5]; }
+__device__ __forceinline__ float sl_value(uint32_t c) { return __uint_as_float(dsl(Sliced8::kValue)[c << 5]); }
 __device__ __forceinline__ const float2 *dqt() {
     return reinterpret_cast<const float2 *>(skv_dec_smem + kSmQt);
 }
@@ -194,14 +193,7 @@ __device__ void stage_decoder_tables(const float *qt_g, const uint32_t *phat, ui
             pc[i] = make_float2((float)w_h * (float)p0, (float)w_h * (float)(p1 - p0) * (1.0f / (1u << kPcShift)));
         }
     }
-    if (DT == SKV_E4M3) {
-        uint32_t *sl = reinterpret_cast<uint32_t *>(skv_dec_smem + kSmCode);
-        for (uint32_t i = threadIdx.x; i < 257u * 32u; i += blockDim.x) {
-            sl[kSlEdge + i] = __float_as_uint(edge_from_values<SKV_E4M3>(i >> 5));
-            sl[kSlPhat + i] = phat[i >> 5];
-            if (i < 256u * 32u) sl[kSlValue + i] = __float_as_uint(Codes<SKV_E4M3>::value(i >> 5));
-        }
-    }
+    if (DT == SKV_E4M3) stage_sliced8(skv_dec_smem + kSmCode, phat);
     stage_phi(*reinterpret_cast<Tables *>(skv_dec_smem + kSmPhi));
     __syncthreads();
 }

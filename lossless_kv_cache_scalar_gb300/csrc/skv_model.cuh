@@ -145,6 +145,21 @@ __device__ void stage_phi(PhiTables<WIDE> &t) {
     }
 }
 
+// The e4m3 code tables (edge E(o) and P_hat(o) for o = 0..256, value of each
+// code) lane-sliced in shared memory: entry i of lane l at word 32 i + l, so
+// that the 32 lanes of a warp, each looking up its own code, hit 32 distinct
+// banks (one shared copy makes those lookups collide on banks).
+struct Sliced8 {
+    static constexpr uint32_t kEdge = 0, kPhat = 257u * 32u, kValue = 2u * 257u * 32u;
+    static constexpr uint32_t kWords = kValue + 256u * 32u;
+    const uint32_t *p;   // the tables' base, offset to this lane's slice
+    __device__ __forceinline__ explicit Sliced8(const void *base)
+        : p(reinterpret_cast<const uint32_t *>(base) + (threadIdx.x & 31u)) {}
+    __device__ __forceinline__ float edge(uint32_t o) const { return __uint_as_float(p[kEdge + (o << 5)]); }
+    __device__ __forceinline__ uint32_t phat(uint32_t o) const { return p[kPhat + (o << 5)]; }
+    __device__ __forceinline__ float value(uint32_t c) const { return __uint_as_float(p[kValue + (c << 5)]); }
+};
+
 // Stage the Phi pairs (and, for e4m3, the edges and P_hat) into shared memory.
 template <uint32_t DT, bool WIDE>
 __device__ void stage_tables(PhiTables<WIDE> &t, Tables8 &t8, const uint32_t *__restrict__ phat) {
@@ -157,6 +172,16 @@ __device__ void stage_tables(PhiTables<WIDE> &t, Tables8 &t8, const uint32_t *__
         for (uint32_t b = threadIdx.x; b < 256u; b += blockDim.x) t8.value[b] = Codes<SKV_E4M3>::value(b);
     }
     __syncthreads();
+}
+
+// Fill the lane-sliced e4m3 tables at base (Sliced8::kWords words; no barrier).
+__device__ inline void stage_sliced8(void *base, const uint32_t *__restrict__ phat) {
+    uint32_t *sl = reinterpret_cast<uint32_t *>(base);
+    for (uint32_t i = threadIdx.x; i < 257u * 32u; i += blockDim.x) {
+        sl[Sliced8::kEdge + i] = __float_as_uint(edge_from_values<SKV_E4M3>(i >> 5));
+        sl[Sliced8::kPhat + i] = phat[i >> 5];
+        if (i < 256u * 32u) sl[Sliced8::kValue + i] = __float_as_uint(Codes<SKV_E4M3>::value(i >> 5));
+    }
 }
 
 // -------------------------------------------------------------- model: C(o)
