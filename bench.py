@@ -814,6 +814,8 @@ def e2e_run(coder, w, lay, args, dev, total_bytes):
     return {"value": raw * steps / dt / 1e9, "unit": "GB/s", "seconds": dt, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "layers_per_batch": hc.lpb,
             "encode_host_ms": 1e3 * float(np.median(t_enc)), "decode_host_ms": 1e3 * float(np.median(t_dec)),
+            "step_ms": [round(1e3 * (a + b), 1) for a, b in zip(t_enc, t_dec)],
+            "median_step_gbs": raw / float(np.median([a + b for a, b in zip(t_enc, t_dec)])) / 1e9,
             "timing": "host wall clock around skv_encode_host (host KV, mu -> host bitstream) and "
                       "skv_decode_host (host bitstream, mu -> host KV), copies overlapped with the kernels"}
 
