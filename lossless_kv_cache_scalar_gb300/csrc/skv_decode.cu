@@ -542,6 +542,21 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
 #pragma unroll 1
         for (uint32_t wi = 0; wi < 4u; ++wi, rse += PER) {
             uint32_t *sw = stage + wi * 32u + lane;
+            // the word's PER values of 1/sigma in one vector load (one gather
+            // per word instead of per code: the lanes' channels lie 32 or 64
+            // bytes apart, so each scalar load touched 32 sectors)
+            float rsv[PER];
+            if constexpr (PER == 2) {
+                const float2 t = __ldg(reinterpret_cast<const float2 *>(rse));
+                rsv[0] = t.x;
+                rsv[1] = t.y;
+            } else {
+                const float4 t = __ldg(reinterpret_cast<const float4 *>(rse));
+                rsv[0] = t.x;
+                rsv[1] = t.y;
+                rsv[2] = t.z;
+                rsv[3] = t.w;
+            }
 #pragma unroll
             for (uint32_t pi = 0; pi < PER; ++pi) {
                 uint32_t slot = 0, o = 0, c = 0, f = 1;
@@ -551,7 +566,7 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
                     const uint32_t mc = BITS == 16 ? (uint32_t)reinterpret_cast<const uint16_t *>(sw)[pi]
                                                    : (uint32_t)reinterpret_cast<const uint8_t *>(sw)[pi];
                     mu = DT == SKV_E4M3 ? sl_value(mc) : K::value(mc);
-                    rs = __ldg(rse + pi);
+                    rs = rsv[pi];
                     const uint32_t om = K::ord(mc);
                     const float ph = phat_est<DT>(a, om);
                     slot = (uint32_t)x & (M - 1u);
