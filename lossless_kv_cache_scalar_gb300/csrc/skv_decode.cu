@@ -227,17 +227,16 @@ __device__ __forceinline__ uint32_t phat_dec(const DecArgs &a, uint32_t o) {
     return Codes<SKV_BF16>::phat(nullptr, a.phat, o);
 }
 
-// Round a value to the nearest code (ties to even), clamped to the finite codes.
+// Round a value to the nearest code (ties to even) and take its order. No
+// clamp to the finite codes: every order indexes the tables (o + 1 <= N), and
+// an estimate on a non-finite code is only a miss for the exact test (a
+// clamp measured 1-1.4% slower).
 template <uint32_t DT> __device__ __forceinline__ uint32_t nearest_ord(float x);
 template <> __device__ __forceinline__ uint32_t nearest_ord<SKV_BF16>(float x) {
-    const uint32_t code = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x));
-    const uint32_t o = Codes<SKV_BF16>::ord(code);
-    return min(max(o, 0x0080u), 0xFF7Fu);
+    return Codes<SKV_BF16>::ord((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x)));
 }
 template <> __device__ __forceinline__ uint32_t nearest_ord<SKV_E4M3>(float x) {
-    const uint32_t code = (uint32_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
-    const uint32_t o = Codes<SKV_E4M3>::ord(code & 0xFFu);
-    return min(max(o, 0x01u), 0xFEu);
+    return Codes<SKV_E4M3>::ord((uint32_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3) & 0xFFu);
 }
 
 // One estimate of the code of slot s, with p_hat's share and the floor term
@@ -273,10 +272,7 @@ __device__ __forceinline__ Estimate estimate(const DecArgs &a, float kS, float i
     r.zt = fmaf(u - (float)k, e.y, e.x);
     r.dz = e.y * (float)kQuantSteps;
     const float xv = fmaf(r.below ? r.zt : -r.zt, sigma, mu);
-    // bf16's first pass is never the answer (a second pass or the saturated
-    // inverse follows), and any order indexes the tables: no clamp needed
-    if (DT == SKV_BF16) r.o = Codes<SKV_BF16>::ord((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xv)));
-    else r.o = nearest_ord<DT>(xv);
+    r.o = nearest_ord<DT>(xv);
     return r;
 }
 
