@@ -147,9 +147,9 @@ class ClockSampler:
         os.unlink(self.path)
         inside = [r for r in rows if self.t0 is not None and self.t1 is not None and self.t0 <= r[0] <= self.t1]
         window = "timed region"
-        if not inside:      # a region shorter than the sampling period: the nearest sample after its start
-            after = [r for r in rows if self.t0 is None or r[0] >= self.t0]
-            inside, window = after[:1], "first sample after the timed region began"
+        if not inside and rows:     # a region shorter than the sampling period: the sample nearest to it
+            mid = 0.5 * (self.t0 + self.t1) if self.t0 is not None and self.t1 is not None else rows[-1][0]
+            inside, window = [min(rows, key=lambda r: abs(r[0] - mid))], "sample nearest to the timed region"
         return {"sm_mhz": statistics.median(r[1] for r in inside) if inside else None,
                 "sm_max_mhz": max(r[2] for r in inside) if inside else None,
                 "samples": len(inside), "window": window,
