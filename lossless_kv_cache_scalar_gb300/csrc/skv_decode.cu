@@ -540,7 +540,8 @@ __device__ __forceinline__ void decode_group(const DecArgs &a, uint64_t gid, uin
             uint32_t *sw = stage + wi * 32u + lane;
             // the word's PER values of 1/sigma in one vector load (one gather
             // per word instead of per code: the lanes' channels lie 32 or 64
-            // bytes apart, so each scalar load touched 32 sectors)
+            // bytes apart, so each scalar load touched 32 sectors); aligned,
+            // since a vector's channel is a multiple of V and rows are HD apart
             float rsv[PER];
             if constexpr (PER == 2) {
                 const float2 t = __ldg(reinterpret_cast<const float2 *>(rse));
