@@ -105,6 +105,16 @@ def test_geometries_bitexact(W, Tc, T):
     H.assert_same_stream(H.layout_of(cfg, tokens_per_chunk=Tc, streams_per_chunk=W), wd, wh)
 
 
+@pytest.mark.parametrize("W,Tc,T", [(32, 256, 300), (96, 100, 257), (256, 7, 20), (128, 1, 3),
+                                    (256, 256, 513)])
+def test_e4m3_geometries_bitexact(W, Tc, T):
+    """The same ragged geometries for e4m3 (16 codes per vector; the decoder's
+    lane-sliced code tables and per-word 1/sigma loads), against the oracle."""
+    cfg = synth.CONFIGS["fp8_32b"].scaled(n_layers=1, n_tokens=T, n_heads=2, head_dim=64, seed=400 + W + T)
+    wd, wh = _workload(cfg)
+    H.assert_same_stream(H.layout_of(cfg, tokens_per_chunk=Tc, streams_per_chunk=W), wd, wh)
+
+
 def test_empty_input():
     lay = Layout("bf16", 2, 2, 8, 128, 0)
     c = Coder(lay)
